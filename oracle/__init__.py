@@ -1,0 +1,162 @@
+"""fp64 CPU oracle for exact softmax attention (forward).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its CPU-baseline leg and ``--impl reference``) may import this
+package.  The product path (``exact_attention_51_gb300``) never imports it and
+shares no code with it; the two meet only through the seeded input generator
+in ``exact_attention_51_gb300.workloads``, which holds none of the method's
+arithmetic.
+
+The arithmetic lives in ``attn_ref.c`` (plain three-pass definition, fp64,
+OpenMP over rows).  This module builds it with gcc on first use and marshals
+numpy / torch-CPU arrays through ctypes.
+
+Sources: "Tri Dao: prediction" (podcast transcript: exact attention, the
+softmax row dependency, the online-softmax trick reaching the same answer);
+HN item 40939030, FlashAttention-3 thread (softmax of the triangular matrix).
+
+Parity status: pinned -- see ``tests/test_oracle.py`` for the pins.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``src`` with gcc -O2 -fopenmp into ``out`` (shared object).
+
+    Plain portable C: no -march flags, so the same source builds on x86_64 and
+    aarch64 hosts.  Returns the path of the library.
+    """
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib):
+    lib.attn_ref_f64.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                 _dbl, ctypes.c_int, ctypes.c_int]
+    lib.attn_ref_f64.restype = ctypes.c_int
+    lib.attn_ref_bf16.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                  _dbl, ctypes.c_int, ctypes.c_int]
+    lib.attn_ref_bf16.restype = ctypes.c_int
+    lib.attn_ref_bf16_rows.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _dbl,
+                                       ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+    lib.attn_ref_bf16_rows.restype = ctypes.c_int
+    lib.attn_ref_max_threads.argtypes = []
+    lib.attn_ref_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library; ``path`` loads another
+    build of an oracle source (the mutation tests use this)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _as_bf16_bits(t) -> np.ndarray:
+    """torch bf16 CPU tensor -> contiguous uint16 numpy view of its bits."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+        raise TypeError("expected a torch.bfloat16 CPU tensor")
+    if t.device.type != "cpu":
+        raise TypeError("oracle inputs live on the CPU")
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _shape4(a):
+    if a.ndim != 4:
+        raise ValueError("expected [B,H,N,d]")
+    return a.shape
+
+
+class Oracle:
+    """Callable wrapper around one build of the oracle library."""
+
+    def __init__(self, lib=None):
+        self.lib = lib if lib is not None else load()
+
+    def max_threads(self) -> int:
+        return int(self.lib.attn_ref_max_threads())
+
+    def attn_f64(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
+        """fp64 inputs [B,H,N,d] (numpy) -> (o fp64 [B,H,N,d], lse fp64 [B,H,N])."""
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        B, H, N, d = _shape4(q)
+        if k.shape != q.shape or v.shape != q.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        o = np.empty((B, H, N, d), np.float64)
+        lse = np.empty((B, H, N), np.float64)
+        rc = self.lib.attn_ref_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                   o.ctypes.data, lse.ctypes.data, B, H, N, d,
+                                   float(scale), int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_f64 failed: {rc}")
+        return o, lse
+
+    def attn_bf16(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
+        """torch bf16 CPU [B,H,N,d] -> (o fp64, lse fp64), whole tensors."""
+        qb, kb, vb = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        B, H, N, d = _shape4(qb)
+        if kb.shape != qb.shape or vb.shape != qb.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        o = np.empty((B, H, N, d), np.float64)
+        lse = np.empty((B, H, N), np.float64)
+        rc = self.lib.attn_ref_bf16(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
+                                    o.ctypes.data, lse.ctypes.data, B, H, N, d,
+                                    float(scale), int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_bf16 failed: {rc}")
+        return o, lse
+
+    def attn_bf16_rows(self, q, k, v, causal: bool, scale: float, rows,
+                       nthreads: int = 0):
+        """Selected flat rows ((b*H+h)*N + i) -> (o fp64 [R,d], lse fp64 [R])."""
+        qb, kb, vb = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        B, H, N, d = _shape4(qb)
+        if kb.shape != qb.shape or vb.shape != qb.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        R = rows.shape[0]
+        o = np.empty((max(R, 1), d), np.float64)
+        lse = np.empty((max(R, 1),), np.float64)
+        rc = self.lib.attn_ref_bf16_rows(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
+                                         B, H, N, d, float(scale), int(bool(causal)),
+                                         rows.ctypes.data, R, o.ctypes.data,
+                                         lse.ctypes.data, int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_bf16_rows failed: {rc}")
+        return o[:R], lse[:R]
+
+
+def default() -> Oracle:
+    return Oracle()

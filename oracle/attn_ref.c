@@ -1,0 +1,252 @@
+/*
+ * Exact softmax attention, forward, in plain fp64 -- the ORACLE.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or helper with the CUDA
+ * path under exact_attention_51_gb300/csrc.
+ *
+ * What it computes (the plain definition, not the tiled algorithm):
+ *
+ *   s_ij  = scale * sum_c q_ic k_jc                     for visible j
+ *   m_i   = max_j s_ij                                  (pass 1)
+ *   l_i   = sum_j exp(s_ij - m_i)                       (pass 2)
+ *   o_ic  = sum_j exp(s_ij - m_i) v_jc / l_i            (pass 3)
+ *   lse_i = m_i + ln l_i
+ *
+ * "visible j" is every key 0..N-1, or 0..i when causal (the lower
+ * "triangular matrix" of the scores; key j is visible to query i iff j <= i,
+ * with Nq = Nk = N, so the diagonal is always visible and no row is empty).
+ *
+ * Sources: "Tri Dao: prediction" (highsignal podcast transcript) -- exact
+ * attention whose softmax needs a sum across the row of the attention matrix,
+ * which the fused method must still reproduce exactly ("still get the right
+ * answer"); "FlashAttention-3" HN thread -- the softmax of the triangular
+ * matrix (causal mask).  The online-softmax rescaling the fast path uses is
+ * NOT reproduced here: the oracle is the three-pass definition the rescaling
+ * has to agree with.
+ *
+ * Inputs are bf16 bit patterns (what the GPU reads) decoded here by a 16-bit
+ * shift into the high half of an IEEE binary32, or plain fp64 arrays (used by
+ * the pin tests).  Layout: contiguous [B,H,N,d] row-major for q, k, v, o and
+ * [B,H,N] for lse.  All arithmetic is fp64 with libm exp/log.
+ *
+ * Parity status: pinned (tiled-vs-two-pass brute force, closed forms,
+ * invariants and a library cross-check; see tests/test_oracle.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+/* bf16 -> fp64: the 16 stored bits are the top half of a binary32. */
+static double bf16_bits_to_f64(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One query row against one head's keys and values (all fp64, row-major
+ * [N,d]).  `s` is caller-provided scratch of N doubles.
+ */
+static void attend_row(const double *q_i, const double *K, const double *V,
+                       int64_t N, int64_t d, int64_t i, double scale,
+                       int causal, double *s, double *o_i, double *lse_i) {
+    int64_t last = causal ? i : N - 1; /* visible keys are 0..last */
+
+    /* scores */
+    for (int64_t j = 0; j <= last; ++j) {
+        const double *k_j = K + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += q_i[c] * k_j[c];
+        s[j] = scale * acc;
+    }
+    /* pass 1: row maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= last; ++j)
+        if (s[j] > m) m = s[j];
+    /* pass 2: normaliser; s is overwritten with exp(s - m) */
+    double l = 0.0;
+    for (int64_t j = 0; j <= last; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    /* pass 3: probability-weighted sum of value rows */
+    for (int64_t c = 0; c < d; ++c) o_i[c] = 0.0;
+    for (int64_t j = 0; j <= last; ++j) {
+        const double p = s[j] / l;
+        const double *v_j = V + j * d;
+        for (int64_t c = 0; c < d; ++c) o_i[c] += p * v_j[c];
+    }
+    *lse_i = m + log(l);
+}
+
+static int check_sizes(int64_t B, int64_t H, int64_t N, int64_t d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return ORACLE_EINVAL;
+    /* keep B*H*N*d well inside int64 */
+    if ((double)B * (double)H * (double)N * (double)d > 4.0e18) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/*
+ * Rows of one head: `rows` lists query indices i (0..N-1) of head (b,h);
+ * outputs go to o_out[r*d..] and lse_out[r] for the r-th listed row.
+ * K, V (and Q rows) are fp64 [N,d] of that head.
+ */
+static int head_rows(const double *Qh, const double *Kh, const double *Vh,
+                     int64_t N, int64_t d, double scale, int causal,
+                     const int64_t *rows, int64_t nrows, double *o_out,
+                     double *lse_out) {
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)N * sizeof(double));
+        if (!s) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (!s) continue;
+            const int64_t i = rows ? rows[r] : r;
+            attend_row(Qh + i * d, Kh, Vh, N, d, i, scale, causal, s,
+                       o_out + r * d, lse_out + r);
+        }
+        free(s);
+    }
+    return err ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- fp64 in */
+
+/* Whole tensors, fp64 inputs. */
+int attn_ref_f64(const double *q, const double *k, const double *v, double *o,
+                 double *lse, int64_t B, int64_t H, int64_t N, int64_t d,
+                 double scale, int causal, int nthreads) {
+    if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
+    int rc = check_sizes(B, H, N, d);
+    if (rc) return rc;
+    set_threads(nthreads);
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const int64_t off = bh * N * d;
+        rc = head_rows(q + off, k + off, v + off, N, d, scale, causal, NULL, N,
+                       o + off, lse + bh * N);
+        if (rc) return rc;
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- bf16 in */
+
+static void decode_head(const uint16_t *src, double *dst, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) dst[t] = bf16_bits_to_f64(src[t]);
+}
+
+/*
+ * Selected rows, bf16 inputs.  rows[r] is a flat row id (b*H + h)*N + i and
+ * may come in any order; the r-th result goes to o_rows[r*d..] and
+ * lse_rows[r].  Each head that owns at least one listed row is decoded to
+ * fp64 once per call.
+ */
+int attn_ref_bf16_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       int64_t B, int64_t H, int64_t N, int64_t d, double scale,
+                       int causal, const int64_t *rows, int64_t nrows,
+                       double *o_rows, double *lse_rows, int nthreads) {
+    if (!q || !k || !v || !rows || !o_rows || !lse_rows || nrows < 0)
+        return ORACLE_EINVAL;
+    int rc = check_sizes(B, H, N, d);
+    if (rc) return rc;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= B * H * N) return ORACLE_EINVAL;
+    set_threads(nthreads);
+
+    const size_t head_elems = (size_t)N * (size_t)d;
+    double *Qh = (double *)malloc(head_elems * sizeof(double));
+    double *Kh = (double *)malloc(head_elems * sizeof(double));
+    double *Vh = (double *)malloc(head_elems * sizeof(double));
+    int64_t *sel = (int64_t *)malloc((size_t)(nrows ? nrows : 1) * sizeof(int64_t));
+    int64_t *pos = (int64_t *)malloc((size_t)(nrows ? nrows : 1) * sizeof(int64_t));
+    double *o_tmp = (double *)malloc((size_t)(nrows ? nrows : 1) * (size_t)d * sizeof(double));
+    double *l_tmp = (double *)malloc((size_t)(nrows ? nrows : 1) * sizeof(double));
+    if (!Qh || !Kh || !Vh || !sel || !pos || !o_tmp || !l_tmp) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
+        int64_t cnt = 0;
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] / N == bh) {
+                sel[cnt] = rows[r] % N;
+                pos[cnt] = r;
+                ++cnt;
+            }
+        if (cnt == 0) continue;
+        const int64_t off = bh * (int64_t)head_elems;
+        decode_head(q + off, Qh, (int64_t)head_elems);
+        decode_head(k + off, Kh, (int64_t)head_elems);
+        decode_head(v + off, Vh, (int64_t)head_elems);
+        rc = head_rows(Qh, Kh, Vh, N, d, scale, causal, sel, cnt, o_tmp, l_tmp);
+        for (int64_t t = 0; t < cnt && rc == ORACLE_OK; ++t) {
+            memcpy(o_rows + pos[t] * d, o_tmp + t * d, (size_t)d * sizeof(double));
+            lse_rows[pos[t]] = l_tmp[t];
+        }
+    }
+done:
+    free(Qh); free(Kh); free(Vh); free(sel); free(pos); free(o_tmp); free(l_tmp);
+    return rc;
+}
+
+/* Whole tensors, bf16 inputs. */
+int attn_ref_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  double *o, double *lse, int64_t B, int64_t H, int64_t N,
+                  int64_t d, double scale, int causal, int nthreads) {
+    if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
+    int rc = check_sizes(B, H, N, d);
+    if (rc) return rc;
+    set_threads(nthreads);
+    const size_t head_elems = (size_t)N * (size_t)d;
+    double *Qh = (double *)malloc(head_elems * sizeof(double));
+    double *Kh = (double *)malloc(head_elems * sizeof(double));
+    double *Vh = (double *)malloc(head_elems * sizeof(double));
+    if (!Qh || !Kh || !Vh) {
+        free(Qh); free(Kh); free(Vh);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
+        const int64_t off = bh * (int64_t)head_elems;
+        decode_head(q + off, Qh, (int64_t)head_elems);
+        decode_head(k + off, Kh, (int64_t)head_elems);
+        decode_head(v + off, Vh, (int64_t)head_elems);
+        rc = head_rows(Qh, Kh, Vh, N, d, scale, causal, NULL, N, o + off,
+                       lse + bh * N);
+    }
+    free(Qh); free(Kh); free(Vh);
+    return rc;
+}
+
+/* Threads OpenMP will use for a parallel region (1 without OpenMP). */
+int attn_ref_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
