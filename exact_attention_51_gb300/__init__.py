@@ -1,0 +1,154 @@
+"""GB300-native fused exact attention forward (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/attn_fwd.h`` (library
+``libexact_attn_gb300.so`` built in place by ``exact_attention_51_gb300.build``).
+Every step of the computation runs in the CUDA kernels behind ``attn_fwd``;
+this module only marshals torch tensors (device memory) and the current CUDA
+stream into the C call.  There is no CPU fallback: without the built library
+every call raises.
+
+    O   = softmax(scale * Q K^T [+ causal mask]) V      (bf16 [B,H,N,d])
+    LSE = ln sum_j exp(scale * q_i . k_j)                (fp32 [B,H,N])
+
+Sources: "Tri Dao: prediction" (fusion, tiling, online softmax); "Show HN:
+Flash Attention in ~100 lines of CUDA" (forward pass, torch only for
+bindings); HN item 40939030 (causal = softmax of the triangular matrix).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libexact_attn_gb300.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_MISALIGNED = 2
+ATTN_ERR_ALIAS = 3
+ATTN_ERR_UNSUPPORTED_DEVICE = 4
+ATTN_ERR_LAUNCH = 5
+ATTN_ERR_TIMEOUT = 6
+
+SUPPORTED_HEAD_DIMS = (64, 128, 256)
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+_flt = ctypes.c_float
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {attn_status_string(status)} (status {status})")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA extension (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA extension {path} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(or python -m exact_attention_51_gb300.build)")
+        lib = ctypes.CDLL(path)
+        lib.attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _flt, _int, _vp]
+        lib.attn_fwd.restype = _int
+        lib.attn_fwd_check_args.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _flt,
+                                            _int]
+        lib.attn_fwd_check_args.restype = _int
+        lib.attn_status_string.argtypes = [_int]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_fwd_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.attn_fwd_device_status.restype = _int
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_last_cuda_error.restype = _int
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def attn_last_cuda_error() -> int:
+    return int(load_library().attn_last_cuda_error())
+
+
+def attn_fwd_check_args(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int,
+                        H: int, N: int, d: int, scale: float, causal: bool) -> int:
+    """Host-only argument checks on raw pointers (never dereferenced)."""
+    return int(load_library().attn_fwd_check_args(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N,
+                                                  d, float(scale), int(bool(causal))))
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             stream=None):
+    """Fused attention forward on CUDA bf16 tensors [B, H, N, d].
+
+    Returns ``(o, lse)``: o bf16 [B,H,N,d], lse fp32 [B,H,N] (natural log,
+    scale included).  ``scale`` defaults to 1/sqrt(d).  ``out`` / ``lse`` may
+    be given to write in place.  The call is asynchronous on ``stream``
+    (default: torch's current stream of q's device).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, d]")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, H, N, d, float(scale), int(bool(causal)),
+                          _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_device_status(stream=None, device=None):
+    """Synchronise the stream, read and clear the device wait-timeout word.
+
+    Returns ``(status, detail)``; status is ATTN_OK or ATTN_ERR_TIMEOUT.
+    """
+    import torch
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    detail = ctypes.c_uint(0)
+    with torch.cuda.device(device):
+        rc = load_library().attn_fwd_device_status(_stream_handle(stream, device),
+                                                   ctypes.byref(detail))
+    return int(rc), int(detail.value)

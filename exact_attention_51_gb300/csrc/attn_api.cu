@@ -1,0 +1,194 @@
+// C ABI of the fused attention forward: argument checks, TMA descriptor
+// encoding and dispatch to the per-head-dim kernels.  The declarations and the
+// contract of every entry point are in include/attn_fwd.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd.h"
+#include "fwd_dispatch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+// Device-wide word the kernels set when a bounded wait gives up.
+__device__ unsigned int g_attn_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  unsigned int* status = nullptr;  // device address of g_attn_status
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_LAUNCH;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+               int H, int N, int d, float scale, int /*causal*/) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  // Launch limits: B*H heads fit the TMA's 32-bit dimension and the grid's
+  // 31-bit x extent (with at least 128 query rows per CTA).
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t ctas = BH * ((static_cast<int64_t>(N) + 127) / 128);
+  if (BH > 0x7fffffffLL || ctas > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
+  if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4)) return ATTN_ERR_MISALIGNED;
+  const size_t tensor_bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * 4;
+  for (const void* in : {q, k, v}) {
+    if (overlaps(o, tensor_bytes, in, tensor_bytes)) return ATTN_ERR_ALIAS;
+    if (overlaps(lse, lse_bytes, in, tensor_bytes)) return ATTN_ERR_ALIAS;
+  }
+  if (overlaps(lse, lse_bytes, o, tensor_bytes)) return ATTN_ERR_ALIAS;
+  return ATTN_OK;
+}
+
+// Per-device set-up: compute capability check and the status word's address.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.checked) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return fail_cuda(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return fail_cuda(e);
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      void* addr = nullptr;
+      if ((e = cudaGetSymbolAddress(&addr, g_attn_status)) != cudaSuccess) return fail_cuda(e);
+      s.status = static_cast<unsigned int*>(addr);
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult qr{};
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &qr);
+      if (e != cudaSuccess) return fail_cuda(e);
+      if (qr != cudaDriverEntryPointSuccess || !fn) return fail_cuda(cudaErrorNotSupported);
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.checked = true;
+  }
+  if (!s.supported) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  *out = &s;
+  return ATTN_OK;
+}
+
+// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); box = 64 columns
+// (one 128-byte swizzle span) x `rows` rows x one head.  Rows past N read as
+// zeros, so a ragged last tile never touches the next head.
+int encode_map(CUtensorMap* map, const void* base, int64_t BH, int N, int d, int rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(N)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, int B, int H, int N, int d, float scale, int causal) {
+  return check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, void* stream) {
+  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (rc != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+
+  const ea51::FwdVariant var = d == 64    ? ea51::fwd_variant_d64()
+                               : d == 128 ? ea51::fwd_variant_d128()
+                                          : ea51::fwd_variant_d256();
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  alignas(64) CUtensorMap tq, tk, tv;
+  if ((rc = encode_map(&tq, q, BH, N, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
+
+  ea51::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.status = ds->status;
+  p.N = N;
+  p.BH = static_cast<int>(BH);
+  p.n_qblk = (N + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const cudaError_t e =
+      var.launch(&tq, &tk, &tv, p, causal != 0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer (q/k/v/o need 16 bytes, lse 4)";
+    case ATTN_ERR_ALIAS: return "an output buffer overlaps another buffer";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
+    case ATTN_ERR_LAUNCH: return "CUDA call failed (see attn_last_cuda_error)";
+    case ATTN_ERR_TIMEOUT: return "a device-side wait timed out; outputs are invalid";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd_device_status(void* stream, unsigned int* detail) {
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  unsigned int word = 0, zero = 0;
+  if ((e = cudaMemcpy(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e);
+  if (word != 0 &&
+      (e = cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return fail_cuda(e);
+  if (detail) *detail = word;
+  return word == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,580 @@
+// Fused exact attention forward for sm_103a (GB300).
+//
+// One CTA owns NQ query tiles of 128 rows of one (batch, head) and streams
+// every visible key/value tile of that head through shared memory once:
+//
+//   TMA warp      Q tiles once, then K_j / V_j tiles into a STAGES-deep ring
+//                 (full / empty mbarriers per slot).
+//   MMA warp      one thread issues tcgen05.mma: S = Q K_j^T into tensor
+//                 memory (fp32), later O += P V_j with P read from tensor
+//                 memory (bf16, written over the S columns it came from).
+//   softmax WGs   one warpgroup per query tile, one thread per row: loads the
+//                 S row from tensor memory, applies scale and mask, keeps the
+//                 running row max m and row sum l, writes P = exp2(x - m) as
+//                 bf16 back to tensor memory, and rescales its O row in
+//                 tensor memory when the max grew by more than 2^8.
+//                 The epilogue divides by l and writes O (bf16) and LSE.
+//
+// The N x N score matrix only ever lives in tensor memory, one 128 x BN tile
+// at a time ("Tri Dao: prediction": kernel fusion + tiling into fast memory +
+// the online-softmax rescaling that "still gets the right answer").  Causal
+// runs visit only key tiles at or below the diagonal ("the softmax of the
+// triangular matrix", HN item 40939030) and mask inside diagonal tiles.
+//
+// Every mbarrier wait is bounded (about two seconds); a wait that gives up
+// records a code in a device status word, sets a CTA-wide abort flag, drains
+// its own in-flight copies / MMAs and lets the CTA exit, so a fault in the
+// pipeline cannot hang the GPU.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fwd_dispatch.h"
+#include "ptx.cuh"
+
+namespace ea51 {
+
+constexpr int BM = 128;                      // query rows per tile (tcgen05 M)
+constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O when max grows > 2^8
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// Per-head-dim tiling.  BN = keys per tile, NQ = query tiles per CTA,
+// NSB = S buffers per query tile in tensor memory, STAGES = K/V ring slots.
+template <int D>
+struct Shape;
+template <>
+struct Shape<64> {
+  static constexpr int BN = 128, NQ = 2, NSB = 1, STAGES = 8;
+};
+template <>
+struct Shape<128> {
+  static constexpr int BN = 128, NQ = 2, NSB = 1, STAGES = 4;
+};
+template <>
+struct Shape<256> {
+  static constexpr int BN = 64, NQ = 1, NSB = 2, STAGES = 4;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int BN = Shape<D>::BN, NQ = Shape<D>::NQ, NSB = Shape<D>::NSB,
+                       STAGES = Shape<D>::STAGES;
+  static constexpr int PANELS = D / 64;  // 128-byte (64 x bf16) column panels per row
+  static constexpr int Q_PANEL = BM * 128;
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_PANEL = BN * 128;
+  static constexpr int KV_BYTES = BN * D * 2;
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = NQ * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * KV_BYTES;
+  // barrier indices
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KVFULL = B_QFULL + NQ;
+  static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
+  static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // [NQ][NSB]
+  static constexpr int B_PFULL = B_SFULL + NQ * NSB;  // [NQ][NSB]
+  static constexpr int B_ODONE = B_PFULL + NQ * NSB;  // [NQ]
+  static constexpr int B_OFINAL = B_ODONE + NQ;       // [NQ]
+  static constexpr int B_DRAIN = B_OFINAL + NQ;
+  static constexpr int NBAR = B_DRAIN + 1;
+  static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 4;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
+  // tensor memory columns (fp32 each)
+  static constexpr int TMEM_COLS = 512;
+  __host__ __device__ static constexpr int s_col(int q, int b) { return (q * NSB + b) * BN; }
+  __host__ __device__ static constexpr int o_col(int q) { return NQ * NSB * BN + q * D; }
+  // warps: [0, 4*NQ) softmax warpgroups, then TMA, MMA, two spare warps
+  static constexpr int TMA_WARP = 4 * NQ;
+  static constexpr int MMA_WARP = 4 * NQ + 1;
+  static constexpr int THREADS = (NQ + 1) * 128;
+  // Register split (setmaxnreg) when the launch budget per thread is tight:
+  // 384 threads launch with 168 registers each (65536 / 384, rounded down to
+  // 8).  The control warpgroup drops to 64 and the two softmax warpgroups
+  // rise to 208: 2 * 128 * (208 - 168) = 10240 <= 128 * (168 - 64) = 13312.
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
+  static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : 0;
+  static constexpr int REG_CONTROL = NQ == 2 ? 64 : 0;
+  static_assert(REG_SOFTMAX == 0 ||
+                    NQ * 128 * (REG_SOFTMAX - LAUNCH_REGS) <= 128 * (LAUNCH_REGS - REG_CONTROL),
+                "register split exceeds the launch budget");
+
+  static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
+  static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1024-byte tile alignment");
+};
+
+// ------------------------------------------------------------ bounded waits
+
+struct Waiter {
+  volatile uint32_t* abort_flag;  // shared memory, CTA-wide
+  unsigned int* status;           // global, device-wide
+};
+
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Waiter w, uint32_t code,
+                                       bool honour_abort) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort) {
+      if (*w.abort_flag) return false;
+      if (*reinterpret_cast<volatile unsigned int*>(w.status) != 0u) {
+        *w.abort_flag = 1u;
+        return false;
+      }
+    }
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      atomicCAS(w.status, 0u, code);
+      *w.abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
+// Wait for the phase of parity `parity`; false if the CTA is aborting.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Waiter w, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, w, code, true);
+}
+
+// Same, for a whole warp: all lanes agree on the outcome.
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, Waiter w,
+                                                uint32_t code) {
+  const bool ok = wait_phase(bar, parity, w, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, Waiter w, uint32_t code) {
+  if (!mbar_try_wait(bar, parity)) wait_slow(bar, parity, w, code, false);
+}
+
+// Diagnostic codes: 0x100 | role << 4 | barrier kind.
+enum : uint32_t {
+  kCodeProducerEmpty = 0x101,
+  kCodeMmaQ = 0x111,
+  kCodeMmaKV = 0x112,
+  kCodeMmaP = 0x113,
+  kCodeSoftS = 0x121,
+  kCodeSoftO = 0x122,
+  kCodeSoftFinal = 0x123,
+  kCodeDrain = 0x131,
+};
+
+// ---------------------------------------------------------------- roles
+
+template <int D, bool CAUSAL>
+struct Tile {
+  int bh;
+  int row0;                   // first query row of the CTA
+  int nkv[Shape<D>::NQ];      // key tiles visited by each query tile (0 = tile absent)
+};
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ Tile<D, CAUSAL> make_tile(const FwdParams& p) {
+  using L = Layout<D>;
+  Tile<D, CAUSAL> t;
+  const int cta = blockIdx.x;
+  t.bh = cta / p.n_qblk;
+  int qblk = cta % p.n_qblk;
+  if (CAUSAL) qblk = p.n_qblk - 1 - qblk;  // heaviest query blocks of a head first
+  t.row0 = qblk * L::NQ * BM;
+  const int nkv_all = (p.N + L::BN - 1) / L::BN;
+#pragma unroll
+  for (int q = 0; q < L::NQ; ++q) {
+    const int r0 = t.row0 + q * BM;
+    if (r0 >= p.N) {
+      t.nkv[q] = 0;
+    } else if (CAUSAL) {
+      const int last_row = min(r0 + BM - 1, p.N - 1);
+      t.nkv[q] = last_row / L::BN + 1;
+    } else {
+      t.nkv[q] = nkv_all;
+    }
+  }
+  return t;
+}
+
+template <int D, bool CAUSAL>
+__device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                              const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL>& t,
+                              Waiter w) {
+  using L = Layout<D>;
+  const uint32_t bar0 = sbase + L::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  int nkv = 0;
+#pragma unroll
+  for (int q = 0; q < L::NQ; ++q) {
+    nkv = max(nkv, t.nkv[q]);
+    if (t.nkv[q] > 0) {
+      const uint32_t fb = bar(L::B_QFULL + q);
+      mbar_arrive_expect_tx(fb, L::Q_BYTES);
+#pragma unroll
+      for (int pn = 0; pn < L::PANELS; ++pn)
+        tma_load_3d(sbase + L::OFF_Q + q * L::Q_BYTES + pn * L::Q_PANEL, tm_q, fb, pn * 64,
+                    t.row0 + q * BM, t.bh);
+    }
+  }
+  const int total = 2 * nkv;  // K_0, V_0, K_1, V_1, ...
+  int issued = 0;
+  for (int i = 0; i < total; ++i) {
+    const int st = i % L::STAGES;
+    const uint32_t ph = static_cast<uint32_t>(i / L::STAGES) & 1u;
+    if (!wait_phase(bar(L::B_KVEMPTY + st), ph ^ 1u, w, kCodeProducerEmpty)) break;
+    const uint32_t fb = bar(L::B_KVFULL + st);
+    mbar_arrive_expect_tx(fb, L::KV_BYTES);
+    const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
+    const int key0 = (i >> 1) * L::BN;
+#pragma unroll
+    for (int pn = 0; pn < L::PANELS; ++pn)
+      tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb, pn * 64, key0,
+                  t.bh);
+    ++issued;
+  }
+  if (*w.abort_flag) {
+    // Let every copy this thread started land before the CTA exits.
+#pragma unroll
+    for (int q = 0; q < L::NQ; ++q)
+      if (t.nkv[q] > 0) drain_phase(bar(L::B_QFULL + q), 0u, w, kCodeDrain);
+    for (int i = max(0, issued - L::STAGES); i < issued; ++i)
+      drain_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u, w,
+                  kCodeDrain);
+  }
+}
+
+template <int D, bool CAUSAL>
+__device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t, Waiter w) {
+  using L = Layout<D>;
+  constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, false);  // A=Q, B=K: both K-major
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, true);    // A=P (tmem), B=V MN-major
+  const uint32_t bar0 = sbase + L::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+
+  bool ok = true;
+  int nkv = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    nkv = max(nkv, t.nkv[q]);
+    if (t.nkv[q] > 0 && ok) ok = wait_phase(bar(L::B_QFULL + q), 0u, w, kCodeMmaQ);
+  }
+
+  // ring slot i holds K_(i/2) (even i) or V_(i/2) (odd i)
+  auto slot_addr = [&](int i) {
+    return sbase + L::OFF_KV + static_cast<uint32_t>((i % L::STAGES) * L::KV_BYTES);
+  };
+  auto wait_full = [&](int i) {
+    return wait_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u,
+                      w, kCodeMmaKV);
+  };
+  auto release = [&](int i) { mma_commit(bar(L::B_KVEMPTY + i % L::STAGES)); };
+
+  // S(q, b) = Q_q K^T with K in ring slot `ks`
+  auto issue_s = [&](int q, int b, int ks) {
+    const uint64_t a0 = sdesc_sw128(sbase + L::OFF_Q + q * L::Q_BYTES, 16, 1024);
+    const uint64_t b0 = sdesc_sw128(slot_addr(ks), 16, 1024);
+    const uint32_t d_t = tmem + L::s_col(q, b);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t ao = ((k / 4) * L::Q_PANEL + (k % 4) * 32) >> 4;
+      const uint32_t bo = ((k / 4) * L::KV_PANEL + (k % 4) * 32) >> 4;
+      mma_ss(d_t, a0 + ao, b0 + bo, kIdescQK, k > 0 ? 1u : 0u);
+    }
+    mma_commit(bar(L::B_SFULL + q * NSB + b));
+  };
+  // O_q (+)= P(q, b) V with V in ring slot `vs`
+  auto issue_pv = [&](int q, int b, int vs, bool accumulate) {
+    const uint64_t b0 = sdesc_sw128(slot_addr(vs), L::KV_PANEL, 1024);
+    const uint32_t d_t = tmem + L::o_col(q);
+    const uint32_t a_t = tmem + L::s_col(q, b);
+#pragma unroll
+    for (int k = 0; k < BN / 16; ++k) {
+      const uint32_t bo = (k * 16 * 128) >> 4;
+      mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u);
+    }
+    mma_commit(bar(L::B_ODONE + q));
+  };
+
+  if (ok) {
+    if constexpr (NSB == 1) {
+      // Per key tile j: PV_q(j) then S_q(j+1) for q = 0, 1, so the tensor
+      // core works on one query tile while the other's softmax runs.
+      ok = wait_full(0);
+      if (ok) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (t.nkv[q] > 0) issue_s(q, 0, 0);
+        release(0);
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        const int vi = 2 * j + 1, ki = 2 * j + 2;
+        ok = wait_full(vi);
+        bool k_ready = false;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!ok || j >= t.nkv[q]) continue;
+          ok = wait_phase(bar(L::B_PFULL + q), static_cast<uint32_t>(j) & 1u, w, kCodeMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          issue_pv(q, 0, vi, j > 0);
+          if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q));
+          if (j + 1 < t.nkv[q]) {
+            if (!k_ready) {
+              ok = wait_full(ki);
+              if (!ok) break;
+              k_ready = true;
+            }
+            issue_s(q, 0, ki);
+          }
+        }
+        if (!ok) break;
+        release(vi);
+        if (k_ready) release(ki);
+      }
+    } else {
+      // One query tile, two S buffers: S(j+2) is computed while the softmax
+      // works on S(j+1) and the tensor core runs PV(j).
+      const int n = t.nkv[0];
+      for (int j = 0; j < 2 && j < n && ok; ++j) {
+        ok = wait_full(2 * j);
+        if (ok) {
+          issue_s(0, j, 2 * j);
+          release(2 * j);
+        }
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int b = j & 1;
+        ok = wait_full(2 * j + 1);
+        if (!ok) break;
+        ok = wait_phase(bar(L::B_PFULL + b), static_cast<uint32_t>(j >> 1) & 1u, w, kCodeMmaP);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv(0, b, 2 * j + 1, j > 0);
+        if (j + 1 == n) mma_commit(bar(L::B_OFINAL));
+        release(2 * j + 1);
+        if (j + 2 < n) {
+          ok = wait_full(2 * (j + 2));
+          if (!ok) break;
+          issue_s(0, b, 2 * (j + 2));
+          release(2 * (j + 2));
+        }
+      }
+    }
+  }
+  if (!ok) {
+    // Let every MMA this thread issued finish before tensor memory is freed.
+    mma_commit(bar(L::B_DRAIN));
+    drain_phase(bar(L::B_DRAIN), 0u, w, kCodeDrain);
+  }
+}
+
+template <int D, bool CAUSAL>
+__device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t,
+                             const FwdParams& p, Waiter w) {
+  using L = Layout<D>;
+  constexpr int BN = L::BN, NSB = L::NSB;
+  constexpr int NCH = BN / 32;  // 32-column chunks of an S row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;  // row inside the query tile == TMEM lane
+  const int r0 = t.row0 + q * BM;
+  const int grow = r0 + r;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t bar0 = sbase + L::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const int n = t.nkv[q];
+  const float c = p.scale_log2;
+  const uint32_t o_t = tmem + lane_base + L::o_col(q);
+
+  float m_used = 0.f;  // exponent offset of P, l and O (log2 units, scale applied)
+  float l = 0.f;
+  bool ok = n > 0;
+  for (int j = 0; j < n && ok; ++j) {
+    const int b = (NSB == 1) ? 0 : (j & 1);
+    const uint32_t sph = static_cast<uint32_t>(NSB == 1 ? j : (j >> 1)) & 1u;
+    ok = warp_wait_phase(bar(L::B_SFULL + q * NSB + b), sph, w, kCodeSoftS);
+    if (!ok) break;
+    tc_fence_after_sync();
+    const uint32_t s_t = tmem + lane_base + L::s_col(q, b);
+    uint32_t s[NCH][32];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld_32x32b_x32(s_t + ch * 32, s[ch]);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) tmem_ld_wait(s[ch]);
+
+    const int key0 = j * BN;
+    const bool masked = (CAUSAL && key0 + BN - 1 > r0) || (key0 + BN > p.N);
+    int lim = BN;  // columns [0, lim) of this tile are visible to this row
+    if (masked) {
+      lim = p.N - key0;
+      if (CAUSAL) lim = min(lim, grow - key0 + 1);
+    }
+
+    // row maximum of the raw scores (scale >= 0 keeps the arg-max)
+    float mx;
+    {
+      float mm[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mm[e] = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x = __uint_as_float(s[ch][e]);
+          const float xv = (!masked || ch * 32 + e < lim) ? x : -INFINITY;
+          mm[e & 7] = fmaxf(mm[e & 7], xv);
+        }
+      mx = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                 fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+    }
+    const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
+
+    if (j == 0) {
+      m_used = (mx_c == -INFINITY) ? 0.f : mx_c;
+    } else {
+      const float m_new = fmaxf(m_used, mx_c);
+      const bool need = m_new > m_used + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        // O holds PV(j-1) once o_done completes its phase j-1.
+        ok = warp_wait_phase(bar(L::B_ODONE + q), static_cast<uint32_t>(j - 1) & 1u, w,
+                             kCodeSoftO);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+        if (need) m_used = m_new;
+        l *= alpha;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(o_t + ch * 32, ov);
+          tmem_ld_wait(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st_32x32b_x32(o_t + ch * 32, ov);
+        }
+        tmem_st_wait();
+      }
+    }
+
+    // P = exp2(x * c - m_used), written over the first BN/2 columns of S
+    const float neg_m = -m_used;
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e]), c, neg_m));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e + 1]), c, neg_m));
+        if (masked) {
+          p0 = (ch * 32 + 2 * e < lim) ? p0 : 0.f;
+          p1 = (ch * 32 + 2 * e + 1 < lim) ? p1 : 0.f;
+        }
+        ls[e & 3] += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      tmem_st_32x32b_x16(s_t + ch * 16, pk);
+    }
+    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::B_PFULL + q * NSB + b));
+  }
+
+  if (!ok) return;
+  // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+  ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
+  if (!ok) return;
+  tc_fence_after_sync();
+  const float inv_l = 1.f / l;
+  const bool valid = grow < p.N;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0)) * D;
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t ov[32];
+    tmem_ld_32x32b_x32(o_t + ch * 32, ov);
+    tmem_ld_wait(ov);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+    if (valid) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+    }
+  }
+  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l)) * kLn2;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Layout<D>::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Tile<D, CAUSAL> t = make_tile<D, CAUSAL>(p);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
+  const Waiter w{abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    const uint32_t bar0 = sbase + L::OFF_BAR;
+    for (int i = 0; i < L::NBAR; ++i) {
+      uint32_t count = 1;
+      if (i >= L::B_PFULL && i < L::B_PFULL + L::NQ * L::NSB) count = 4;  // one per softmax warp
+      mbar_init(bar0 + 8u * i, count);
+    }
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == L::TMA_WARP && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == L::MMA_WARP) {
+    tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  // Each role runs to the end of the kernel on its own path (the register
+  // split differs per path), then meets the others at the teardown barrier.
+  if (warp < 4 * L::NQ) {
+    if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
+    softmax_role<D, CAUSAL>(warp >> 2, tmem, sbase, t, p, w);
+    tc_fence_before_sync();
+    __syncthreads();
+  } else {
+    if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
+    if (warp == L::TMA_WARP) {
+      if (lane == 0) producer_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, t, w);
+      __syncwarp();
+    } else if (warp == L::MMA_WARP) {
+      if (lane == 0) mma_role<D, CAUSAL>(tmem, sbase, t, w);
+      __syncwarp();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == L::MMA_WARP) {
+      tc_fence_after_sync();
+      tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+  }
+}
+
+}  // namespace ea51

@@ -1,0 +1,44 @@
+// Kernel launch for one head dim (both causal flags).  Included by exactly one
+// translation unit per head dim so the three variants compile in parallel.
+#pragma once
+#include <atomic>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace ea51 {
+
+template <int D, bool CAUSAL>
+cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                       const FwdParams& p, cudaStream_t stream) {
+  using L = Layout<D>;
+  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  // The dynamic shared-memory opt-in is per device; remember which are done.
+  static std::atomic<unsigned long long> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const unsigned grid = static_cast<unsigned>(p.n_qblk) * static_cast<unsigned>(p.BH);
+  kern<<<grid, L::THREADS, L::SMEM_ALLOC, stream>>>(*tq, *tk, *tv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                     const FwdParams& p, bool causal, cudaStream_t stream) {
+  return causal ? launch_one<D, true>(tq, tk, tv, p, stream)
+                : launch_one<D, false>(tq, tk, tv, p, stream);
+}
+
+template <int D>
+FwdVariant make_variant() {
+  using L = Layout<D>;
+  return FwdVariant{L::BN, L::NQ * BM, &launch_d<D>};
+}
+
+}  // namespace ea51

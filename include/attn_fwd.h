@@ -1,0 +1,119 @@
+/*
+ * exact_attention_51_gb300 -- C ABI of the fused exact attention forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (all entry points below compute or check this one):
+ *
+ *     O   = softmax(scale * Q K^T  [+ causal mask]) V
+ *     LSE = ln sum_j exp(scale * q_i . k_j)          (over the visible keys j)
+ *
+ * computed exactly -- not approximated -- as ONE fused, tiled kernel: the
+ * N x N score matrix is never written to HBM.  The softmax row dependency is
+ * broken with the online-softmax trick: the kernel visits key/value tiles in
+ * order, keeps a running row maximum and row sum, and rescales the partial
+ * output whenever the maximum grows, which reaches the same result as the
+ * plain three-pass softmax.  Sources: "Tri Dao: prediction" (podcast
+ * transcript: I/O awareness, kernel fusion, tiling into fast memory, the
+ * softmax row dependency and the online-softmax trick); "Show HN: Flash
+ * Attention in ~100 lines of CUDA" (forward pass only; torch used only for
+ * bindings); HN item 40939030, FlashAttention-3 thread (the softmax of the
+ * triangular matrix, i.e. causal attention, and the FA2/FA3/ThunderKittens
+ * prior art).
+ *
+ * Conventions shared by every entry point
+ *   - Q, K, V, O: bf16, contiguous row-major [B, H, N, d] (d fastest), passed
+ *     as device pointers to __nv_bfloat16 data typed void* so that callers
+ *     need no CUDA headers.  Nq = Nk = N (self-attention shapes).
+ *   - LSE: fp32, contiguous [B, H, N], natural logarithm, scale included.
+ *   - d must be 64, 128 or 256.  B, H, N >= 1.
+ *   - scale: finite and >= 0 (the softmax temperature, usually 1/sqrt(d)).
+ *   - causal != 0: key j is visible to query i iff j <= i (top-left aligned
+ *     lower triangle; the diagonal is visible, so no row is empty).
+ *   - Ownership: the caller owns every buffer.  The library allocates no
+ *     device memory per call and keeps no per-call state.
+ *   - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *     Calls are asynchronous: they enqueue work and return without a host
+ *     synchronisation.  Execution errors surface at the caller's next
+ *     synchronisation, as for any CUDA launch.
+ *   - Thread safety: every entry point may be called from several host
+ *     threads at once.
+ */
+#ifndef EXACT_ATTENTION_51_GB300_ATTN_FWD_H
+#define EXACT_ATTENTION_51_GB300_ATTN_FWD_H
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by the entry points. */
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,        /* null pointer, size < 1, d not in {64,128,256},
+                                      sizes whose products overflow the launch,
+                                      non-finite or negative scale */
+  ATTN_ERR_MISALIGNED = 2,         /* q/k/v/o not 16-byte aligned, lse not 4-byte aligned */
+  ATTN_ERR_ALIAS = 3,              /* o or lse overlaps an input, or lse overlaps o */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+  ATTN_ERR_LAUNCH = 5,             /* CUDA runtime/driver call failed; see attn_last_cuda_error */
+  ATTN_ERR_TIMEOUT = 6             /* a device-side wait gave up (see attn_fwd_device_status) */
+};
+
+/*
+ * Fused exact attention forward.
+ *
+ *   q, k, v  device pointers, bf16 [B,H,N,d], read only (they may alias each
+ *            other).  16-byte aligned.
+ *   o        device pointer, bf16 [B,H,N,d], written.  16-byte aligned; must
+ *            not overlap q, k, v or lse.
+ *   lse      device pointer, fp32 [B,H,N], written.  4-byte aligned; must not
+ *            overlap q, k, v or o.
+ *   scale    multiplies Q K^T before the softmax.
+ *   causal   0 = full attention, nonzero = causal (j <= i).
+ *   stream   cudaStream_t to enqueue on.
+ *
+ * Enqueues one kernel and returns.  On any validation error nothing is
+ * launched and the status says why.  O rows are the probability-weighted
+ * value rows rounded to bf16 (round to nearest even); LSE is fp32.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, void* stream);
+
+/*
+ * The host-side argument checks of attn_fwd, without touching the GPU or the
+ * CUDA runtime: returns ATTN_OK or the status attn_fwd would return for these
+ * arguments before its device check.  Pointers are only compared, never
+ * dereferenced.
+ */
+ATTN_API int attn_fwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, int B, int H, int N, int d, float scale, int causal);
+
+/* Static, NUL-terminated English text for a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/*
+ * Every wait inside the kernel is bounded: a wait that does not complete
+ * within about two seconds stops that thread block, records a diagnostic
+ * code in a device-wide status word and lets the kernel return instead of
+ * hanging.  This call synchronises `stream`, reads the status word of the
+ * current device, clears it and returns ATTN_OK (no timeout since the last
+ * call) or ATTN_ERR_TIMEOUT.  `detail`, if not NULL, receives the raw code
+ * (0 when clean).  Outputs of launches that ran while the word was set are
+ * not valid.
+ */
+ATTN_API int attn_fwd_device_status(void* stream, unsigned int* detail);
+
+/* The cudaError_t of the last failed CUDA call made by this host thread
+ * inside the library (0 if none). */
+ATTN_API int attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_51_GB300_ATTN_FWD_H */

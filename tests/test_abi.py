@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports exactly what
+include/*.h declares, and its host-side argument checks reject bad calls
+before anything is launched."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import exact_attention_51_gb300 as ea
+from exact_attention_51_gb300 import build as eabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = "\n".join(l for l in src.splitlines() if not l.lstrip().startswith("#"))
+        for m in re.finditer(r"ATTN_API\s+[\w\s\*]*?\b(\w+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    eabuild.build()
+    return ea.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_check_args", "attn_status_string",
+            "attn_fwd_device_status", "attn_last_cuda_error"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_only_c_abi_is_exported(lib):
+    out = os.popen(f"nm -D --defined-only {ea.LIB_PATH}").read()
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == declared_functions(), exported ^ declared_functions()
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert ea.attn_status_string(code) not in ("", "unknown status")
+    assert ea.attn_status_string(99) == "unknown status"
+
+
+A = 1 << 20  # fake, 16-byte aligned "device" addresses (never dereferenced)
+
+
+def ptrs(n_bytes):
+    base = [A, A + 4 * n_bytes, A + 8 * n_bytes, A + 12 * n_bytes, A + 16 * n_bytes]
+    return base
+
+
+def chk(q, k, v, o, lse, B=1, H=2, N=128, d=64, scale=0.125, causal=0):
+    return ea.attn_fwd_check_args(q, k, v, o, lse, B, H, N, d, scale, causal)
+
+
+def test_check_args_accepts_valid(lib):
+    n = 1 * 2 * 128 * 64 * 2
+    assert chk(*ptrs(n)) == ea.ATTN_OK
+    assert chk(*ptrs(n), causal=1) == ea.ATTN_OK
+    for d in (64, 128, 256):
+        assert chk(*ptrs(1 * 2 * 128 * d * 2), d=d) == ea.ATTN_OK
+    assert chk(*ptrs(n), scale=0.0) == ea.ATTN_OK
+    q = ptrs(n)[0]
+    assert chk(q, q, q, *ptrs(n)[3:]) == ea.ATTN_OK  # inputs may alias each other
+
+
+@pytest.mark.parametrize("field", range(5))
+def test_check_args_null_pointer(lib, field):
+    p = ptrs(1 << 16)
+    p[field] = 0
+    assert chk(*p) == ea.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0), dict(B=-1), dict(d=32),
+                                dict(d=96), dict(d=512), dict(scale=float("nan")),
+                                dict(scale=float("inf")), dict(scale=-0.5),
+                                dict(B=1 << 20, H=1 << 12), dict(B=1 << 16, H=1 << 8, N=1 << 20)])
+def test_check_args_invalid(lib, kw):
+    assert chk(*ptrs(1 << 40), **kw) == ea.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,off", [(0, 8), (1, 2), (2, 4), (3, 8), (4, 2)])
+def test_check_args_misaligned(lib, field, off):
+    p = ptrs(1 << 16)
+    p[field] += off
+    assert chk(*p) == ea.ATTN_ERR_MISALIGNED
+
+
+def test_check_args_alias(lib):
+    n = 1 * 2 * 128 * 64 * 2
+    q, k, v, o, lse = ptrs(n)
+    assert chk(q, k, v, q, lse) == ea.ATTN_ERR_ALIAS          # o == q
+    assert chk(q, k, v, v + 16, lse) == ea.ATTN_ERR_ALIAS     # o overlaps v
+    assert chk(q, k, v, o, k + n - 16) == ea.ATTN_ERR_ALIAS   # lse overlaps k's tail
+    assert chk(q, k, v, o, o + 64) == ea.ATTN_ERR_ALIAS       # lse inside o
+    assert chk(q, k, v, o, o + n) == ea.ATTN_OK               # lse right after o
+
+
+def test_missing_extension_fails_loudly(tmp_path):
+    saved = ea._lib
+    ea._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            ea.load_library(str(tmp_path / "nope.so"))
+    finally:
+        ea._lib = saved
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros((1, 1, 4, 64), dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        ea.attn_fwd(x, x, x)
