@@ -158,24 +158,23 @@ def row_flops(w: wl.Workload, causal: bool, rows) -> float:
 
 
 def time_oracle(w, causal, q, k, v, target_s: float, seed: int):
-    """Oracle throughput (TFLOP/s) on a seeded random row sample sized to take
-    about `target_s` seconds; returns (tflops, seconds, rows, threads)."""
+    """Oracle throughput (TFLOP/s) on seeded random row samples, grown until
+    one sample takes about `target_s` seconds; returns (tflops, seconds, rows,
+    threads)."""
     import numpy as np
     import oracle
     orc = oracle.Oracle()
     rng = np.random.default_rng(seed)
     total_rows = w.B * w.H * w.N
-    probe = sorted(rng.choice(total_rows, size=64, replace=False).tolist())
-    t0 = time.perf_counter()
-    orc.attn_bf16_rows(q, k, v, causal, w.scale, probe)
-    dt = time.perf_counter() - t0
-    per_row = max(dt / 64, 1e-6)
-    n = int(min(total_rows, max(64, target_s / per_row)))
-    rows = sorted(rng.choice(total_rows, size=n, replace=False).tolist())
-    t0 = time.perf_counter()
-    orc.attn_bf16_rows(q, k, v, causal, w.scale, rows)
-    dt = time.perf_counter() - t0
-    return row_flops(w, causal, rows) / dt / 1e12, dt, n, orc.max_threads()
+    n = 256
+    while True:
+        rows = sorted(rng.choice(total_rows, size=min(n, total_rows), replace=False).tolist())
+        t0 = time.perf_counter()
+        orc.attn_bf16_rows(q, k, v, causal, w.scale, rows)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or len(rows) == total_rows:
+            return row_flops(w, causal, rows) / dt / 1e12, dt, len(rows), orc.max_threads()
+        n = int(len(rows) * min(8.0, max(1.5, target_s / max(dt, 1e-3))))
 
 
 # ---------------------------------------------------------------- main arms
@@ -198,11 +197,16 @@ def run_reference(args, w, causal):
     rng = np.random.default_rng(12345)
     total_rows = w.B * w.H * w.N
     # size each step to ~2 s of oracle work so K + W steps stay within minutes
-    probe = sorted(rng.choice(total_rows, size=32, replace=False).tolist())
-    t0 = time.perf_counter()
-    orc.attn_bf16_rows(q, k, v, causal, w.scale, probe)
-    per_row = max((time.perf_counter() - t0) / 32, 1e-6)
-    n = int(min(total_rows, max(32, 2.0 / per_row)))
+    n = 256
+    while True:
+        rows = sorted(rng.choice(total_rows, size=min(n, total_rows), replace=False).tolist())
+        t0 = time.perf_counter()
+        orc.attn_bf16_rows(q, k, v, causal, w.scale, rows)
+        dt = time.perf_counter() - t0
+        if dt >= 1.0 or len(rows) == total_rows:
+            break
+        n = int(len(rows) * min(8.0, max(1.5, 2.0 / max(dt, 1e-3))))
+    n = len(rows)
     times, flops = [], []
     for step in range(args.warmup + args.steps):
         rows = sorted(rng.choice(total_rows, size=n, replace=False).tolist())

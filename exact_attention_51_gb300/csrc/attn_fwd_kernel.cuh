@@ -390,8 +390,13 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   const float c = p.scale_log2;
   const uint32_t o_t = tmem + lane_base + L::o_col(q);
 
-  float m_used = 0.f;  // exponent offset of P, l and O (log2 units, scale applied)
-  float l = 0.f;
+  // Running state of this row, all in log2 units with the scale applied:
+  // m_used is the exponent offset of P, l_exact = sum of the fp32 p (for LSE),
+  // l_round = sum of the bf16-rounded p that actually multiply V (for O, so
+  // the weights applied to V are normalised exactly; the rounding error of a
+  // dominant weight then cancels between numerator and denominator).
+  float m_used = 0.f;
+  float l_exact = 0.f, l_round = 0.f;
   bool ok = n > 0;
   for (int j = 0; j < n && ok; ++j) {
     const int b = (NSB == 1) ? 0 : (j & 1);
@@ -417,19 +422,19 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     // row maximum of the raw scores (scale >= 0 keeps the arg-max)
     float mx;
     {
-      float mm[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mm[e] = -INFINITY;
+      float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = __uint_as_float(s[ch][e]);
-          const float xv = (!masked || ch * 32 + e < lim) ? x : -INFINITY;
-          mm[e & 7] = fmaxf(mm[e & 7], xv);
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(s[ch][e]), x1 = __uint_as_float(s[ch][e + 1]);
+          if (masked) {
+            x0 = (ch * 32 + e < lim) ? x0 : -INFINITY;
+            x1 = (ch * 32 + e + 1 < lim) ? x1 : -INFINITY;
+          }
+          mm[(e >> 1) & 3] = fmax3(mm[(e >> 1) & 3], x0, x1);
         }
-      mx = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                 fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+      mx = fmax3(fmaxf(mm[0], mm[1]), mm[2], mm[3]);
     }
     const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
 
@@ -446,7 +451,8 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
         tc_fence_after_sync();
         const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
         if (need) m_used = m_new;
-        l *= alpha;
+        l_exact *= alpha;
+        l_round *= alpha;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t ov[32];
@@ -460,26 +466,34 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       }
     }
 
-    // P = exp2(x * c - m_used), written over the first BN/2 columns of S
-    const float neg_m = -m_used;
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of S
+    const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m_used, -m_used);
+    f32x2 le[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+    f32x2 lr[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e]), c, neg_m));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[ch][2 * e + 1]), c, neg_m));
+        const f32x2 x = f2_fma(f2_pack(__uint_as_float(s[ch][2 * e]),
+                                       __uint_as_float(s[ch][2 * e + 1])), cc, nm);
+        float t0, t1;
+        f2_unpack(x, t0, t1);
+        float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
         if (masked) {
           p0 = (ch * 32 + 2 * e < lim) ? p0 : 0.f;
           p1 = (ch * 32 + 2 * e + 1 < lim) ? p1 : 0.f;
         }
-        ls[e & 3] += p0 + p1;
-        pk[e] = pack_bf16x2(p0, p1);
+        const uint32_t pb = pack_bf16x2(p0, p1);
+        pk[e] = pb;
+        le[e & 1] = f2_add(le[e & 1], f2_pack(p0, p1));
+        lr[e & 1] = f2_add(lr[e & 1], f2_pack(__uint_as_float(pb << 16),
+                                              __uint_as_float(pb & 0xffff0000u)));
       }
       tmem_st_32x32b_x16(s_t + ch * 16, pk);
     }
-    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+    l_exact += f2_sum(f2_add(le[0], le[1]));
+    l_round += f2_sum(f2_add(lr[0], lr[1]));
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
@@ -491,7 +505,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
   if (!ok) return;
   tc_fence_after_sync();
-  const float inv_l = 1.f / l;
+  const float inv_l = 1.f / l_round;
   const bool valid = grow < p.N;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0)) * D;
 #pragma unroll
@@ -510,7 +524,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
         dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
     }
   }
-  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l)) * kLn2;
+  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l_exact)) * kLn2;
 }
 
 template <int D, bool CAUSAL>

@@ -8,6 +8,9 @@ O_gpu is bf16, LSE_gpu fp32; the oracle is fp64 on the same bf16 inputs.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 O_MAX_ABS = 2e-2
@@ -43,3 +46,11 @@ def describe(m) -> str:
     return (f"o_max_abs={m['o_max_abs']:.3e} (<= {O_MAX_ABS}) o_rel_rms={m['o_rel_rms']:.3e} "
             f"(<= {O_REL_RMS}) lse_max_abs={m['lse_max_abs']:.3e} (<= {LSE_MAX_ABS}) "
             f"finite={m['finite']} o_argmax={m['o_argmax']} lse_argmax={m['lse_argmax']}")
+
+
+def record(label: str, m) -> None:
+    """Append the metrics of one case to $PARITY_LOG (JSON lines), if set."""
+    path = os.environ.get("PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": label, **m}) + "\n")

@@ -16,7 +16,7 @@ import torch
 import exact_attention_51_gb300 as ea
 import oracle
 from exact_attention_51_gb300 import workloads as wl
-from parity import describe, metrics, within
+from parity import describe, metrics, record, within
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,7 @@ def check_full(q, k, v, causal, scale=None, label=""):
     o, lse = run_gpu(q, k, v, causal, scale)
     o_ref, lse_ref = orc().attn_bf16(q, k, v, causal, scale)
     m = metrics(o, o_ref, lse, lse_ref)
+    record(f"{label} {tuple(q.shape)} causal={causal} scale={scale:.4g}", m)
     assert within(m), f"{label} {tuple(q.shape)} causal={causal}: {describe(m)}"
     return m
 
@@ -203,6 +204,7 @@ def test_workload_sampled_rows(name, causal):
     o_s = o.reshape(-1, w.d)[rows]
     l_s = lse.reshape(-1)[rows]
     m = metrics(o_s, o_ref, l_s, lse_ref)
+    record(f"workload {w.describe(causal)} ({len(rows)} sampled rows)", m)
     assert within(m), f"{w.describe(causal)}: {describe(m)}"
     # properties that hold at any size, checked on every row
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
