@@ -119,7 +119,7 @@ static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, 
                                        bool honour_abort) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort) {
       if (*w.abort_flag) return false;
@@ -373,6 +373,59 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
   }
 }
 
+// Row maximum of raw scores; MASKED keeps only columns [0, lim).
+template <int NCH, bool MASKED>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[NCH][32], int lim) {
+  float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float x0 = __uint_as_float(s[ch][e]), x1 = __uint_as_float(s[ch][e + 1]);
+      if (MASKED) {
+        x0 = (ch * 32 + e < lim) ? x0 : -INFINITY;
+        x1 = (ch * 32 + e + 1 < lim) ? x1 : -INFINITY;
+      }
+      mm[(e >> 1) & 3] = fmax3(mm[(e >> 1) & 3], x0, x1);
+    }
+  return fmax3(fmaxf(mm[0], mm[1]), mm[2], mm[3]);
+}
+
+// p = exp2(s * c - m) for one S row, stored as packed bf16 pairs over the
+// first NCH * 16 columns at `s_t`; returns the sums of the fp32 p and of the
+// bf16-rounded p.  MASKED zeroes columns >= lim.
+template <int NCH, bool MASKED>
+__device__ __forceinline__ void exp_store(const uint32_t (&s)[NCH][32], int lim, float c, float m,
+                                          uint32_t s_t, float& sum_exact, float& sum_round) {
+  const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m, -m);
+  f32x2 le[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+  f32x2 lr[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const f32x2 x =
+          f2_fma(f2_pack(__uint_as_float(s[ch][2 * e]), __uint_as_float(s[ch][2 * e + 1])), cc, nm);
+      float t0, t1;
+      f2_unpack(x, t0, t1);
+      float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+      if (MASKED) {
+        p0 = (ch * 32 + 2 * e < lim) ? p0 : 0.f;
+        p1 = (ch * 32 + 2 * e + 1 < lim) ? p1 : 0.f;
+      }
+      const uint32_t pb = pack_bf16x2(p0, p1);
+      pk[e] = pb;
+      le[e & 1] = f2_add(le[e & 1], f2_pack(p0, p1));
+      lr[e & 1] = f2_add(lr[e & 1],
+                         f2_pack(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)));
+    }
+    tmem_st_32x32b_x16(s_t + ch * 16, pk);
+  }
+  sum_exact = f2_sum(f2_add(le[0], le[1]));
+  sum_round = f2_sum(f2_add(lr[0], lr[1]));
+}
+
 template <int D, bool CAUSAL>
 __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t,
                              const FwdParams& p, Waiter w) {
@@ -420,22 +473,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     }
 
     // row maximum of the raw scores (scale >= 0 keeps the arg-max)
-    float mx;
-    {
-      float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0 = __uint_as_float(s[ch][e]), x1 = __uint_as_float(s[ch][e + 1]);
-          if (masked) {
-            x0 = (ch * 32 + e < lim) ? x0 : -INFINITY;
-            x1 = (ch * 32 + e + 1 < lim) ? x1 : -INFINITY;
-          }
-          mm[(e >> 1) & 3] = fmax3(mm[(e >> 1) & 3], x0, x1);
-        }
-      mx = fmax3(fmaxf(mm[0], mm[1]), mm[2], mm[3]);
-    }
+    const float mx = masked ? row_max<NCH, true>(s, lim) : row_max<NCH, false>(s, lim);
     const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
 
     if (j == 0) {
@@ -467,33 +505,13 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     }
 
     // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of S
-    const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m_used, -m_used);
-    f32x2 le[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-    f32x2 lr[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const f32x2 x = f2_fma(f2_pack(__uint_as_float(s[ch][2 * e]),
-                                       __uint_as_float(s[ch][2 * e + 1])), cc, nm);
-        float t0, t1;
-        f2_unpack(x, t0, t1);
-        float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-        if (masked) {
-          p0 = (ch * 32 + 2 * e < lim) ? p0 : 0.f;
-          p1 = (ch * 32 + 2 * e + 1 < lim) ? p1 : 0.f;
-        }
-        const uint32_t pb = pack_bf16x2(p0, p1);
-        pk[e] = pb;
-        le[e & 1] = f2_add(le[e & 1], f2_pack(p0, p1));
-        lr[e & 1] = f2_add(lr[e & 1], f2_pack(__uint_as_float(pb << 16),
-                                              __uint_as_float(pb & 0xffff0000u)));
-      }
-      tmem_st_32x32b_x16(s_t + ch * 16, pk);
-    }
-    l_exact += f2_sum(f2_add(le[0], le[1]));
-    l_round += f2_sum(f2_add(lr[0], lr[1]));
+    float add_exact, add_round;
+    if (masked)
+      exp_store<NCH, true>(s, lim, c, m_used, s_t, add_exact, add_round);
+    else
+      exp_store<NCH, false>(s, lim, c, m_used, s_t, add_exact, add_round);
+    l_exact += add_exact;
+    l_round += add_round;
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
