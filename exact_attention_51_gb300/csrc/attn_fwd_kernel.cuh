@@ -35,7 +35,11 @@
 namespace ea51 {
 
 constexpr int BM = 128;                      // query rows per tile (tcgen05 M)
-constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale O when max grows > 2^8
+// log2 units: O and l are rescaled only when a row's max grows by more than
+// this; otherwise P keeps the old exponent offset (values up to 2^1).  A
+// larger threshold skips more rescales but lets a dominant weight be rounded
+// to bf16 (relative error up to 2^-8) where a fresh offset would make it 1.0.
+constexpr float kRescaleThreshold = 1.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
@@ -119,7 +123,7 @@ static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, 
                                        bool honour_abort) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort) {
       if (*w.abort_flag) return false;
@@ -392,14 +396,13 @@ __device__ __forceinline__ float row_max(const uint32_t (&s)[NCH][32], int lim) 
 }
 
 // p = exp2(s * c - m) for one S row, stored as packed bf16 pairs over the
-// first NCH * 16 columns at `s_t`; returns the sums of the fp32 p and of the
-// bf16-rounded p.  MASKED zeroes columns >= lim.
+// first NCH * 16 columns at `s_t`; returns the sum of the fp32 p.  MASKED
+// zeroes columns >= lim.
 template <int NCH, bool MASKED>
-__device__ __forceinline__ void exp_store(const uint32_t (&s)[NCH][32], int lim, float c, float m,
-                                          uint32_t s_t, float& sum_exact, float& sum_round) {
+__device__ __forceinline__ float exp_store(const uint32_t (&s)[NCH][32], int lim, float c, float m,
+                                           uint32_t s_t) {
   const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m, -m);
-  f32x2 le[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-  f32x2 lr[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+  f32x2 acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     uint32_t pk[16];
@@ -414,16 +417,12 @@ __device__ __forceinline__ void exp_store(const uint32_t (&s)[NCH][32], int lim,
         p0 = (ch * 32 + 2 * e < lim) ? p0 : 0.f;
         p1 = (ch * 32 + 2 * e + 1 < lim) ? p1 : 0.f;
       }
-      const uint32_t pb = pack_bf16x2(p0, p1);
-      pk[e] = pb;
-      le[e & 1] = f2_add(le[e & 1], f2_pack(p0, p1));
-      lr[e & 1] = f2_add(lr[e & 1],
-                         f2_pack(__uint_as_float(pb << 16), __uint_as_float(pb & 0xffff0000u)));
+      pk[e] = pack_bf16x2(p0, p1);
+      acc[e & 1] = f2_add(acc[e & 1], f2_pack(p0, p1));
     }
     tmem_st_32x32b_x16(s_t + ch * 16, pk);
   }
-  sum_exact = f2_sum(f2_add(le[0], le[1]));
-  sum_round = f2_sum(f2_add(lr[0], lr[1]));
+  return f2_sum(f2_add(acc[0], acc[1]));
 }
 
 template <int D, bool CAUSAL>
@@ -443,13 +442,10 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   const float c = p.scale_log2;
   const uint32_t o_t = tmem + lane_base + L::o_col(q);
 
-  // Running state of this row, all in log2 units with the scale applied:
-  // m_used is the exponent offset of P, l_exact = sum of the fp32 p (for LSE),
-  // l_round = sum of the bf16-rounded p that actually multiply V (for O, so
-  // the weights applied to V are normalised exactly; the rounding error of a
-  // dominant weight then cancels between numerator and denominator).
+  // Running state of this row (log2 units, scale applied): m_used is the
+  // exponent offset of P, O and l; l is the sum of the fp32 p.
   float m_used = 0.f;
-  float l_exact = 0.f, l_round = 0.f;
+  float l = 0.f;
   bool ok = n > 0;
   for (int j = 0; j < n && ok; ++j) {
     const int b = (NSB == 1) ? 0 : (j & 1);
@@ -489,8 +485,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
         tc_fence_after_sync();
         const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
         if (need) m_used = m_new;
-        l_exact *= alpha;
-        l_round *= alpha;
+        l *= alpha;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t ov[32];
@@ -505,13 +500,8 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     }
 
     // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of S
-    float add_exact, add_round;
-    if (masked)
-      exp_store<NCH, true>(s, lim, c, m_used, s_t, add_exact, add_round);
-    else
-      exp_store<NCH, false>(s, lim, c, m_used, s_t, add_exact, add_round);
-    l_exact += add_exact;
-    l_round += add_round;
+    l += masked ? exp_store<NCH, true>(s, lim, c, m_used, s_t)
+                : exp_store<NCH, false>(s, lim, c, m_used, s_t);
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
@@ -523,7 +513,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
   if (!ok) return;
   tc_fence_after_sync();
-  const float inv_l = 1.f / l_round;
+  const float inv_l = 1.f / l;
   const bool valid = grow < p.N;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0)) * D;
 #pragma unroll
@@ -542,7 +532,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
         dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
     }
   }
-  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l_exact)) * kLn2;
+  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l)) * kLn2;
 }
 
 template <int D, bool CAUSAL>

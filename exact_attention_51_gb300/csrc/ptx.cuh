@@ -42,18 +42,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
-// True once the phase with parity `parity` has completed.  The thread may be
-// suspended in hardware for up to `suspend_ns` while the phase is pending (it
-// resumes as soon as the phase completes), which keeps waiting warps from
-// spending issue slots on polling.
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
-                                              uint32_t suspend_ns = 0x100000u) {
+// True once the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.b32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
