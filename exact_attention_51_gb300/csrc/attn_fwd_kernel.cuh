@@ -251,6 +251,9 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   }
 }
 
+// Runs on a whole warp with warp-uniform control flow (so the descriptors
+// stay in uniform registers); one elected lane issues every tcgen05.mma and
+// tcgen05.commit.
 template <int D, bool CAUSAL>
 __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t, Waiter w) {
   using L = Layout<D>;
@@ -259,13 +262,14 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
   constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, true);    // A=P (tmem), B=V MN-major
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t leader = elect_one();
 
   bool ok = true;
   int nkv = 0;
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     nkv = max(nkv, t.nkv[q]);
-    if (t.nkv[q] > 0 && ok) ok = wait_phase(bar(L::B_QFULL + q), 0u, w, kCodeMmaQ);
+    if (t.nkv[q] > 0 && ok) ok = warp_wait_phase(bar(L::B_QFULL + q), 0u, w, kCodeMmaQ);
   }
 
   // ring slot i holds K_(i/2) (even i) or V_(i/2) (odd i)
@@ -273,10 +277,10 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
     return sbase + L::OFF_KV + static_cast<uint32_t>((i % L::STAGES) * L::KV_BYTES);
   };
   auto wait_full = [&](int i) {
-    return wait_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u,
-                      w, kCodeMmaKV);
+    return warp_wait_phase(bar(L::B_KVFULL + i % L::STAGES),
+                           static_cast<uint32_t>(i / L::STAGES) & 1u, w, kCodeMmaKV);
   };
-  auto release = [&](int i) { mma_commit(bar(L::B_KVEMPTY + i % L::STAGES)); };
+  auto release = [&](int i) { mma_commit(bar(L::B_KVEMPTY + i % L::STAGES), leader); };
 
   // S(q, b) = Q_q K^T with K in ring slot `ks`
   auto issue_s = [&](int q, int b, int ks) {
@@ -287,9 +291,9 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t ao = ((k / 4) * L::Q_PANEL + (k % 4) * 32) >> 4;
       const uint32_t bo = ((k / 4) * L::KV_PANEL + (k % 4) * 32) >> 4;
-      mma_ss(d_t, a0 + ao, b0 + bo, kIdescQK, k > 0 ? 1u : 0u);
+      mma_ss(d_t, a0 + ao, b0 + bo, kIdescQK, k > 0 ? 1u : 0u, leader);
     }
-    mma_commit(bar(L::B_SFULL + q * NSB + b));
+    mma_commit(bar(L::B_SFULL + q * NSB + b), leader);
   };
   // O_q (+)= P(q, b) V with V in ring slot `vs`
   auto issue_pv = [&](int q, int b, int vs, bool accumulate) {
@@ -299,9 +303,9 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k) {
       const uint32_t bo = (k * 16 * 128) >> 4;
-      mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u);
+      mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u, leader);
     }
-    mma_commit(bar(L::B_ODONE + q));
+    mma_commit(bar(L::B_ODONE + q), leader);
   };
 
   if (ok) {
@@ -322,11 +326,11 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           if (!ok || j >= t.nkv[q]) continue;
-          ok = wait_phase(bar(L::B_PFULL + q), static_cast<uint32_t>(j) & 1u, w, kCodeMmaP);
+          ok = warp_wait_phase(bar(L::B_PFULL + q), static_cast<uint32_t>(j) & 1u, w, kCodeMmaP);
           if (!ok) break;
           tc_fence_after_sync();
           issue_pv(q, 0, vi, j > 0);
-          if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q));
+          if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q), leader);
           if (j + 1 < t.nkv[q]) {
             if (!k_ready) {
               ok = wait_full(ki);
@@ -355,11 +359,12 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
         const int b = j & 1;
         ok = wait_full(2 * j + 1);
         if (!ok) break;
-        ok = wait_phase(bar(L::B_PFULL + b), static_cast<uint32_t>(j >> 1) & 1u, w, kCodeMmaP);
+        ok = warp_wait_phase(bar(L::B_PFULL + b), static_cast<uint32_t>(j >> 1) & 1u, w,
+                             kCodeMmaP);
         if (!ok) break;
         tc_fence_after_sync();
         issue_pv(0, b, 2 * j + 1, j > 0);
-        if (j + 1 == n) mma_commit(bar(L::B_OFINAL));
+        if (j + 1 == n) mma_commit(bar(L::B_OFINAL), leader);
         release(2 * j + 1);
         if (j + 2 < n) {
           ok = wait_full(2 * (j + 2));
@@ -371,8 +376,8 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
     }
   }
   if (!ok) {
-    // Let every MMA this thread issued finish before tensor memory is freed.
-    mma_commit(bar(L::B_DRAIN));
+    // Let every MMA this warp issued finish before tensor memory is freed.
+    mma_commit(bar(L::B_DRAIN), leader);
     drain_phase(bar(L::B_DRAIN), 0u, w, kCodeDrain);
   }
 }
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
       if (lane == 0) producer_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, t, w);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
-      if (lane == 0) mma_role<D, CAUSAL>(tmem, sbase, t, w);
+      mma_role<D, CAUSAL>(tmem, sbase, t, w);
       __syncwarp();
     }
     tc_fence_before_sync();

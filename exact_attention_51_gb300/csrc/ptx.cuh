@@ -132,31 +132,44 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 // --------------------------------------------------------------- tcgen05.mma
 
-// D[tmem] (+)= A[smem] * B[smem]^T-or-not per `idesc`; one thread issues.
+// One lane of the calling (converged) warp: 1 there, 0 elsewhere.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.b32 %0, 1, 0, e;\n\t}"
+               : "=r"(r));
+  return r;
+}
+
+// D[tmem] (+)= A[smem] * B[smem] per `idesc`.  Executed by a whole warp with
+// control flow uniform across it; only the lane with `issue` != 0 issues.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, i;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 i, %5, 0;\n\t"
+      "@i tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
 
 // Same with the A operand read from tensor memory.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, i;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 i, %5, 0;\n\t"
+      "@i tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
 
-// Arrive once on `bar` when every earlier tcgen05.mma of this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// Arrive once on `bar` when every earlier tcgen05.mma of the issuing lane is
+// done (only the lane with `issue` != 0 commits).
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred i;\n\tsetp.ne.b32 i, %1, 0;\n\t"
+      "@i tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar),
+      "r"(issue)
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate.
