@@ -179,6 +179,23 @@ def time_oracle(w, causal, q, k, v, target_s: float, seed: int):
 
 # ---------------------------------------------------------------- main arms
 
+def reduce_max_over_ranks(values, device):
+    """Element-wise max of `values` over all ranks (identity when not
+    distributed).  The only collective in the benchmark; the data path has
+    none."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return world * flops_per_rank / (slowest_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -346,10 +363,7 @@ def run_ours(args, w, causal):
     d2h = q_h.numel() * 2 + w.B * w.H * w.N * 4
 
     # ---- max over ranks
-    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], dev)
 
     if rank == 0:
         peaks, peak_src = load_peaks()
@@ -357,7 +371,7 @@ def run_ours(args, w, causal):
         traffic = load_traffic(args.workload, causal)
         line = {
             "metric": METRIC,
-            "value": ws * flops / (ms * 1e-3) / 1e12,
+            "value": whole_job_tflops(flops, ws, ms),
             "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms,
@@ -377,7 +391,7 @@ def run_ours(args, w, causal):
                          "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
                          "kernel": f"attn_fwd_kernel<{w.d},{str(causal).lower()}>"},
             "clocks": clocks,
-            "e2e": {"value": ws * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "how": "pinned host buffers; H2D, kernel and D2H on three streams, "

@@ -345,32 +345,41 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
         if (k_ready) release(ki);
       }
     } else {
-      // One query tile, two S buffers: S(j+2) is computed while the softmax
-      // works on S(j+1) and the tensor core runs PV(j).
-      const int n = t.nkv[0];
-      for (int j = 0; j < 2 && j < n && ok; ++j) {
-        ok = wait_full(2 * j);
-        if (ok) {
-          issue_s(0, j, 2 * j);
-          release(2 * j);
-        }
+      // Two S buffers per query tile: S_q(j+2) is computed while the softmax
+      // works on S_q(j+1) and the tensor core runs PV_q(j); with two query
+      // tiles their PV/S pairs interleave as well.
+      for (int jj = 0; jj < 2 && jj < nkv && ok; ++jj) {
+        ok = wait_full(2 * jj);
+        if (!ok) break;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (jj < t.nkv[q]) issue_s(q, jj, 2 * jj);
+        release(2 * jj);
       }
-      for (int j = 0; j < n && ok; ++j) {
+      for (int j = 0; j < nkv && ok; ++j) {
         const int b = j & 1;
-        ok = wait_full(2 * j + 1);
-        if (!ok) break;
-        ok = warp_wait_phase(bar(L::B_PFULL + b), static_cast<uint32_t>(j >> 1) & 1u, w,
-                             kCodeMmaP);
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_pv(0, b, 2 * j + 1, j > 0);
-        if (j + 1 == n) mma_commit(bar(L::B_OFINAL), leader);
-        release(2 * j + 1);
-        if (j + 2 < n) {
-          ok = wait_full(2 * (j + 2));
+        const int vi = 2 * j + 1, ki = 2 * (j + 2);
+        ok = wait_full(vi);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!ok || j >= t.nkv[q]) continue;
+          ok = warp_wait_phase(bar(L::B_PFULL + q * NSB + b), static_cast<uint32_t>(j >> 1) & 1u,
+                               w, kCodeMmaP);
           if (!ok) break;
-          issue_s(0, b, 2 * (j + 2));
-          release(2 * (j + 2));
+          tc_fence_after_sync();
+          issue_pv(q, b, vi, j > 0);
+          if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q), leader);
+        }
+        if (!ok) break;
+        release(vi);
+        if (j + 2 < nkv) {
+          // S(j+2) reuses the buffer whose P the PV above just read
+          ok = wait_full(ki);
+          if (!ok) break;
+#pragma unroll
+          for (int q = 0; q < NQ; ++q)
+            if (j + 2 < t.nkv[q]) issue_s(q, b, ki);
+          release(ki);
         }
       }
     }
