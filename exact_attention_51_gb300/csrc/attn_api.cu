@@ -25,6 +25,7 @@ struct DeviceState {
   bool checked = false;
   bool supported = false;
   unsigned int* status = nullptr;  // device address of g_attn_status
+  int sms = 148;                   // streaming multiprocessors
 };
 
 std::mutex g_mu;
@@ -79,6 +80,8 @@ int device_state(DeviceState** out) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return fail_cuda(e);
     s.supported = (major == 10 && minor == 3);
+    if ((e = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail_cuda(e);
     if (s.supported) {
       void* addr = nullptr;
       if ((e = cudaGetSymbolAddress(&addr, g_attn_status)) != cudaSuccess) return fail_cuda(e);

@@ -65,6 +65,7 @@ struct Layout {
   static constexpr int BN = Shape<D>::BN, NQ = Shape<D>::NQ, NSB = Shape<D>::NSB,
                        STAGES = Shape<D>::STAGES;
   static constexpr int PANELS = D / 64;  // 128-byte (64 x bf16) column panels per row
+  static constexpr bool SPLIT_P = BN >= 128;  // hand P to the MMA warp in two halves
   static constexpr int Q_PANEL = BM * 128;
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_PANEL = BN * 128;
@@ -78,8 +79,8 @@ struct Layout {
   static constexpr int B_KVFULL = B_QFULL + NQ;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // [NQ][NSB]
-  static constexpr int B_PFULL = B_SFULL + NQ * NSB;  // [NQ][NSB]
-  static constexpr int B_ODONE = B_PFULL + NQ * NSB;  // [NQ]
+  static constexpr int B_PFULL = B_SFULL + NQ * NSB;  // [NQ][NSB][2 halves of P]
+  static constexpr int B_ODONE = B_PFULL + NQ * NSB * 2;  // [NQ]
   static constexpr int B_OFINAL = B_ODONE + NQ;       // [NQ]
   static constexpr int B_DRAIN = B_OFINAL + NQ;
   static constexpr int NBAR = B_DRAIN + 1;
@@ -184,9 +185,16 @@ __device__ __forceinline__ Tile<D, CAUSAL> make_tile(const FwdParams& p) {
   using L = Layout<D>;
   Tile<D, CAUSAL> t;
   const int cta = blockIdx.x;
-  t.bh = cta / p.n_qblk;
-  int qblk = cta % p.n_qblk;
-  if (CAUSAL) qblk = p.n_qblk - 1 - qblk;  // heaviest query blocks of a head first
+  int qblk;
+  if (CAUSAL) {
+    // Heaviest query blocks first across all heads (longest-processing-time
+    // order): the light blocks of every head fill the tail of the launch.
+    t.bh = cta % p.BH;
+    qblk = p.n_qblk - 1 - cta / p.BH;
+  } else {
+    t.bh = cta / p.n_qblk;
+    qblk = cta % p.n_qblk;
+  }
   t.row0 = qblk * L::NQ * BM;
   const int nkv_all = (p.N + L::BN - 1) / L::BN;
 #pragma unroll
@@ -295,17 +303,27 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
     }
     mma_commit(bar(L::B_SFULL + q * NSB + b), leader);
   };
-  // O_q (+)= P(q, b) V with V in ring slot `vs`
-  auto issue_pv = [&](int q, int b, int vs, bool accumulate) {
+  // O_q (+)= P(q, b) V with V in ring slot `vs`; waits for each half of P
+  // (keys [0, BN/2) then [BN/2, BN)) before issuing its K-steps.
+  auto issue_pv = [&](int q, int b, int vs, bool accumulate, uint32_t pph) {
     const uint64_t b0 = sdesc_sw128(slot_addr(vs), L::KV_PANEL, 1024);
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
 #pragma unroll
-    for (int k = 0; k < BN / 16; ++k) {
-      const uint32_t bo = (k * 16 * 128) >> 4;
-      mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u, leader);
+    constexpr int NH = L::SPLIT_P ? 2 : 1;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      if (!warp_wait_phase(bar(L::B_PFULL + (q * NSB + b) * 2 + h), pph, w, kCodeMmaP))
+        return false;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int k = h * (BN / 16 / NH); k < (h + 1) * (BN / 16 / NH); ++k) {
+        const uint32_t bo = (k * 16 * 128) >> 4;
+        mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u, leader);
+      }
     }
     mma_commit(bar(L::B_ODONE + q), leader);
+    return true;
   };
 
   if (ok) {
@@ -326,10 +344,8 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           if (!ok || j >= t.nkv[q]) continue;
-          ok = warp_wait_phase(bar(L::B_PFULL + q), static_cast<uint32_t>(j) & 1u, w, kCodeMmaP);
+          ok = issue_pv(q, 0, vi, j > 0, static_cast<uint32_t>(j) & 1u);
           if (!ok) break;
-          tc_fence_after_sync();
-          issue_pv(q, 0, vi, j > 0);
           if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q), leader);
           if (j + 1 < t.nkv[q]) {
             if (!k_ready) {
@@ -363,11 +379,8 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           if (!ok || j >= t.nkv[q]) continue;
-          ok = warp_wait_phase(bar(L::B_PFULL + q * NSB + b), static_cast<uint32_t>(j >> 1) & 1u,
-                               w, kCodeMmaP);
+          ok = issue_pv(q, b, vi, j > 0, static_cast<uint32_t>(j >> 1) & 1u);
           if (!ok) break;
-          tc_fence_after_sync();
-          issue_pv(q, b, vi, j > 0);
           if (j + 1 == t.nkv[q]) mma_commit(bar(L::B_OFINAL + q), leader);
         }
         if (!ok) break;
@@ -409,16 +422,17 @@ __device__ __forceinline__ float row_max(const uint32_t (&s)[NCH][32], int lim) 
   return fmax3(fmaxf(mm[0], mm[1]), mm[2], mm[3]);
 }
 
-// p = exp2(s * c - m) for one S row, stored as packed bf16 pairs over the
-// first NCH * 16 columns at `s_t`; returns the sum of the fp32 p.  MASKED
-// zeroes columns >= lim.
-template <int NCH, bool MASKED>
+// p = exp2(s * c - m) for 32-column chunks [CH0, CH1) of one S row, stored
+// as packed bf16 pairs at columns [CH0 * 16, CH1 * 16) from `s_t` (over the
+// S columns already read); returns the sum of the fp32 p.  MASKED zeroes
+// columns >= lim.
+template <int NCH, int CH0, int CH1, bool MASKED>
 __device__ __forceinline__ float exp_store(const uint32_t (&s)[NCH][32], int lim, float c, float m,
                                            uint32_t s_t) {
   const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m, -m);
   f32x2 acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-  for (int ch = 0; ch < NCH; ++ch) {
+  for (int ch = CH0; ch < CH1; ++ch) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -513,13 +527,25 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       }
     }
 
-    // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of S
-    l += masked ? exp_store<NCH, true>(s, lim, c, m_used, s_t)
-                : exp_store<NCH, false>(s, lim, c, m_used, s_t);
+    // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of
+    // S.  With 128-key tiles it is handed to the MMA warp in two halves, so
+    // P.V starts before the second half is computed; 64-key tiles send it
+    // whole (the second barrier round trip costs more than it overlaps).
+    constexpr int H = L::SPLIT_P ? NCH / 2 : NCH;
+    l += masked ? exp_store<NCH, 0, H, true>(s, lim, c, m_used, s_t)
+                : exp_store<NCH, 0, H, false>(s, lim, c, m_used, s_t);
+    if constexpr (L::SPLIT_P) {
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2));
+      l += masked ? exp_store<NCH, H, NCH, true>(s, lim, c, m_used, s_t)
+                  : exp_store<NCH, H, NCH, false>(s, lim, c, m_used, s_t);
+    }
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::B_PFULL + q * NSB + b));
+    if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2 + (L::SPLIT_P ? 1 : 0)));
   }
 
   if (!ok) return;
@@ -568,7 +594,7 @@ __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
     const uint32_t bar0 = sbase + L::OFF_BAR;
     for (int i = 0; i < L::NBAR; ++i) {
       uint32_t count = 1;
-      if (i >= L::B_PFULL && i < L::B_PFULL + L::NQ * L::NSB) count = 4;  // one per softmax warp
+      if (i >= L::B_PFULL && i < L::B_PFULL + L::NQ * L::NSB * 2) count = 4;  // per softmax warp
       mbar_init(bar0 + 8u * i, count);
     }
     *abort_flag = 0u;
