@@ -280,8 +280,22 @@ def run_ours(args, w, causal):
             dist.barrier()
 
     # ---- device-resident timing
+    splits = args.splits
+    if splits == 0:
+        splits = ea.attn_fwd_splitkv_num_splits(
+            w.B, w.H, w.N, w.d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)
+    ws_bytes = ea.attn_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, splits) if splits > 1 else 0
+    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def fwd(qq, kk, vv, oo, ll, st=None):
+        if splits > 1:
+            ea.attn_fwd_splitkv(qq, kk, vv, causal=causal, num_splits=splits, out=oo, lse=ll,
+                                workspace=workspace, stream=st)
+        else:
+            ea.attn_fwd(qq, kk, vv, causal=causal, out=oo, lse=ll, stream=st)
+
     for _ in range(args.warmup):
-        ea.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+        fwd(q, k, v, o, lse)
     torch.cuda.synchronize(dev)
     st, detail = ea.attn_fwd_device_status()
     if st != ea.ATTN_OK:
@@ -295,7 +309,7 @@ def run_ours(args, w, causal):
     t_host0 = time.monotonic()
     ev0.record(stream)
     for _ in range(args.steps):
-        ea.attn_fwd(q, k, v, causal=causal, out=o, lse=lse)
+        fwd(q, k, v, o, lse)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.monotonic()
@@ -335,7 +349,7 @@ def run_ours(args, w, causal):
             b["v"].copy_(vp, non_blocking=True)
             ev_in[i % 2].record(s_h2d)
         stream.wait_event(ev_in[i % 2])
-        ea.attn_fwd(b["q"], b["k"], b["v"], causal=causal, out=b["o"], lse=b["l"], stream=stream)
+        fwd(b["q"], b["k"], b["v"], b["o"], b["l"], stream)
         ev_done[i % 2].record(stream)
         s_d2h.wait_event(ev_done[i % 2])
         with torch.cuda.stream(s_d2h):
@@ -384,7 +398,8 @@ def run_ours(args, w, causal):
                        "causal": causal, "scale": w.scale,
                        "l2": "inputs larger than L2 (3 x %d MiB bf16), no flush" % (
                            q_h.numel() * 2 >> 20),
-                       "parallelism": f"replicas x{ws} (independent batches, no collective)"},
+                       "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                       "kv_splits": splits},
             "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
@@ -396,7 +411,7 @@ def run_ours(args, w, causal):
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "how": "pinned host buffers; H2D, kernel and D2H on three streams, "
                            "double-buffered across steps"},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if splits > 1 else 1),
         }
         if ws == 1 and not args.no_cpu_baseline:
             tf, secs, nrows, cores = time_oracle(w, causal, q_h, k_h, v_h, args.cpu_seconds, 99)
@@ -420,6 +435,9 @@ def main(argv=None):
     ap.add_argument("--causal", choices=["default", "0", "1"], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=1,
+                    help="1: attn_fwd; >1: attn_fwd_splitkv with that many key splits; "
+                         "0: attn_fwd_splitkv with its default split count")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -72,6 +72,13 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_device_status.restype = _int
         lib.attn_last_cuda_error.argtypes = []
         lib.attn_last_cuda_error.restype = _int
+        lib.attn_fwd_splitkv.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _flt,
+                                         _int, _int, _vp, ctypes.c_size_t, _vp]
+        lib.attn_fwd_splitkv.restype = _int
+        lib.attn_fwd_splitkv_workspace_size.argtypes = [_int, _int, _int, _int, _int]
+        lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_splitkv_num_splits.argtypes = [_int, _int, _int, _int, _int, _int]
+        lib.attn_fwd_splitkv_num_splits.restype = _int
         _lib = lib
         return lib
 
@@ -96,6 +103,75 @@ def _stream_handle(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd_splitkv_workspace_size(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    return int(load_library().attn_fwd_splitkv_workspace_size(B, H, N, d, num_splits))
+
+
+def attn_fwd_splitkv_num_splits(B: int, H: int, N: int, d: int, causal: bool,
+                                num_sms: int) -> int:
+    return int(load_library().attn_fwd_splitkv_num_splits(B, H, N, d, int(bool(causal)),
+                                                           num_sms))
+
+
+def _check_qkv(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, d]")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+
+
+def _outputs(q, out, lse):
+    import torch
+    B, H, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
+    return out, lse
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                     num_splits: int | None = None, out=None, lse=None, workspace=None,
+                     stream=None):
+    """Split-KV forward (same result as ``attn_fwd``).  ``num_splits`` None
+    picks one from the shape and the SM count; the workspace is allocated
+    with torch unless given (a uint8 CUDA tensor of enough bytes)."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = attn_fwd_splitkv_num_splits(B, H, N, d, causal, sms)
+    out, lse = _outputs(q, out, lse)
+    need = attn_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                  int(num_splits), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv")
+    return out, lse
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -133,22 +133,27 @@ int attn_fwd_check_args(const void* q, const void* k, const void* v, const void*
   return check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-             int d, float scale, int causal, void* stream) {
-  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
-  if (rc != ATTN_OK) return rc;
-  DeviceState* ds = nullptr;
-  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+}  // extern "C"
 
-  const ea51::FwdVariant var = d == 64    ? ea51::fwd_variant_d64()
-                               : d == 128 ? ea51::fwd_variant_d128()
-                                          : ea51::fwd_variant_d256();
+namespace {
+
+ea51::FwdVariant variant_for(int d) {
+  return d == 64 ? ea51::fwd_variant_d64() : d == 128 ? ea51::fwd_variant_d128()
+                                                      : ea51::fwd_variant_d256();
+}
+
+// Encodes the TMA maps and launches the fused kernel; with kv_splits > 1 the
+// kernel writes partials to o_part / lse_part.
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+               int d, float scale, int causal, int kv_splits, float* o_part, float* lse_part,
+               DeviceState* ds, cudaStream_t stream) {
+  const ea51::FwdVariant var = variant_for(d);
   const int64_t BH = static_cast<int64_t>(B) * H;
   alignas(64) CUtensorMap tq, tk, tv;
+  int rc;
   if ((rc = encode_map(&tq, q, BH, N, d, 128)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tk, k, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tv, v, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
-
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
@@ -157,8 +162,101 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.BH = static_cast<int>(BH);
   p.n_qblk = (N + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  const cudaError_t e =
-      var.launch(&tq, &tk, &tv, p, causal != 0, static_cast<cudaStream_t>(stream));
+  p.kv_splits = kv_splits;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  const cudaError_t e = var.launch(&tq, &tk, &tv, p, causal != 0, stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
+}
+
+constexpr int kMaxSplits = 64;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Bytes of split-KV workspace: fp32 partial O, then fp32 partial LSE.
+size_t splitkv_bytes(int64_t BH, int N, int d, int splits, size_t* lse_offset) {
+  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N);
+  const size_t o_bytes = align256(static_cast<size_t>(splits) * rows * d * 4);
+  if (lse_offset) *lse_offset = o_bytes;
+  return o_bytes + align256(static_cast<size_t>(splits) * rows * 4);
+}
+
+int check_splitkv(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  int B, int H, int N, int d, float scale, int causal, int splits,
+                  const void* ws, size_t ws_bytes) {
+  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (rc != ATTN_OK) return rc;
+  if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH * ((static_cast<int64_t>(N) + 127) / 128) * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (splits == 1) return ATTN_OK;
+  const size_t need = splitkv_bytes(BH, N, d, splits, nullptr);
+  if (!ws || ws_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_MISALIGNED;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2, lb = static_cast<size_t>(BH) * N * 4;
+  if (overlaps(ws, need, q, tb) || overlaps(ws, need, k, tb) || overlaps(ws, need, v, tb) ||
+      overlaps(ws, need, o, tb) || overlaps(ws, need, lse, lb))
+    return ATTN_ERR_ALIAS;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, void* stream) {
+  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (rc != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  return launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, nullptr, ds,
+                    static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (d != 64 && d != 128 && d != 256) return 0;
+  if (num_splits == 1) return 0;
+  return splitkv_bytes(static_cast<int64_t>(B) * H, N, d, num_splits, nullptr);
+}
+
+int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1) return 1;
+  const ea51::FwdVariant var = variant_for(d);
+  const int64_t ctas = static_cast<int64_t>(B) * H * ((N + var.q_rows_per_cta - 1) / var.q_rows_per_cta);
+  const int64_t key_tiles = (static_cast<int64_t>(N) + var.kv_rows - 1) / var.kv_rows;
+  // Split only while the launch fills less than one wave, keeping at least
+  // four key tiles per share (causal blocks see about half the keys).
+  if (ctas >= num_sms) return 1;
+  int64_t s = (num_sms + ctas - 1) / ctas;
+  const int64_t max_by_tiles = (causal ? key_tiles / 2 : key_tiles) / 4;
+  if (s > max_by_tiles) s = max_by_tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, int num_splits, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int rc = check_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+                         workspace_bytes);
+  if (rc != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (num_splits == 1)
+    return launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, nullptr, ds, st);
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  size_t lse_off = 0;
+  splitkv_bytes(BH, N, d, num_splits, &lse_off);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
+  if ((rc = launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, o_part, lse_part, ds,
+                       st)) != ATTN_OK)
+    return rc;
+  const cudaError_t e = ea51::launch_combine(d, o_part, lse_part, o, lse, BH * N, num_splits, st);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTN_OK;
 }

@@ -173,18 +173,22 @@ enum : uint32_t {
 
 // ---------------------------------------------------------------- roles
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 struct Tile {
   int bh;
   int row0;                   // first query row of the CTA
-  int nkv[Shape<D>::NQ];      // key tiles visited by each query tile (0 = tile absent)
+  int split;                  // which share of the key tiles (split-KV), 0 otherwise
+  int lo;                     // first key tile of this CTA's share
+  int nkv[Shape<D>::NQ];      // key tiles [lo, lo + nkv) visited by each query tile
 };
 
-template <int D, bool CAUSAL>
-__device__ __forceinline__ Tile<D, CAUSAL> make_tile(const FwdParams& p) {
+template <int D, bool CAUSAL, bool SPLIT>
+__device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) {
   using L = Layout<D>;
-  Tile<D, CAUSAL> t;
-  const int cta = blockIdx.x;
+  Tile<D, CAUSAL, SPLIT> t;
+  const int splits = SPLIT ? p.kv_splits : 1;
+  const int cta = blockIdx.x / splits;
+  t.split = blockIdx.x - cta * splits;
   int qblk;
   if (CAUSAL) {
     // Heaviest query blocks first across all heads (longest-processing-time
@@ -197,24 +201,33 @@ __device__ __forceinline__ Tile<D, CAUSAL> make_tile(const FwdParams& p) {
   }
   t.row0 = qblk * L::NQ * BM;
   const int nkv_all = (p.N + L::BN - 1) / L::BN;
+  int nkv_abs[L::NQ];
+  int nkv_cta = 0;
 #pragma unroll
   for (int q = 0; q < L::NQ; ++q) {
     const int r0 = t.row0 + q * BM;
     if (r0 >= p.N) {
-      t.nkv[q] = 0;
+      nkv_abs[q] = 0;
     } else if (CAUSAL) {
       const int last_row = min(r0 + BM - 1, p.N - 1);
-      t.nkv[q] = last_row / L::BN + 1;
+      nkv_abs[q] = last_row / L::BN + 1;
     } else {
-      t.nkv[q] = nkv_all;
+      nkv_abs[q] = nkv_all;
     }
+    nkv_cta = max(nkv_cta, nkv_abs[q]);
   }
+  // split-KV: an even share of the CTA's key tiles
+  const int per = (nkv_cta + splits - 1) / splits;
+  t.lo = min(t.split * per, nkv_cta);
+  const int hi = min(t.lo + per, nkv_cta);
+#pragma unroll
+  for (int q = 0; q < L::NQ; ++q) t.nkv[q] = max(0, min(hi, nkv_abs[q]) - t.lo);
   return t;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                              const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL>& t,
+                              const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                               Waiter w) {
   using L = Layout<D>;
   const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -241,7 +254,7 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     const uint32_t fb = bar(L::B_KVFULL + st);
     mbar_arrive_expect_tx(fb, L::KV_BYTES);
     const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
-    const int key0 = (i >> 1) * L::BN;
+    const int key0 = (t.lo + (i >> 1)) * L::BN;
 #pragma unroll
     for (int pn = 0; pn < L::PANELS; ++pn)
       tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb, pn * 64, key0,
@@ -262,8 +275,8 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 // Runs on a whole warp with warp-uniform control flow (so the descriptors
 // stay in uniform registers); one elected lane issues every tcgen05.mma and
 // tcgen05.commit.
-template <int D, bool CAUSAL>
-__device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t, Waiter w) {
+template <int D, bool CAUSAL, bool SPLIT>
+__device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t, Waiter w) {
   using L = Layout<D>;
   constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, false);  // A=Q, B=K: both K-major
@@ -326,7 +339,7 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t
     return true;
   };
 
-  if (ok) {
+  if (ok && nkv > 0) {  // nkv == 0: an empty split-KV share, nothing to issue
     if constexpr (NSB == 1) {
       // Per key tile j: PV_q(j) then S_q(j+1) for q = 0, 1, so the tensor
       // core works on one query tile while the other's softmax runs.
@@ -453,8 +466,8 @@ __device__ __forceinline__ float exp_store(const uint32_t (&s)[NCH][32], int lim
   return f2_sum(f2_add(acc[0], acc[1]));
 }
 
-template <int D, bool CAUSAL>
-__device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL>& t,
+template <int D, bool CAUSAL, bool SPLIT>
+__device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                              const FwdParams& p, Waiter w) {
   using L = Layout<D>;
   constexpr int BN = L::BN, NSB = L::NSB;
@@ -474,7 +487,14 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   // exponent offset of P, O and l; l is the sum of the fp32 p.
   float m_used = 0.f;
   float l = 0.f;
-  bool ok = n > 0;
+  if (n == 0) {
+    // This split saw no key of this query tile: an empty partial.
+    if (SPLIT && grow < p.N)
+      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.N + static_cast<size_t>(t.bh) * p.N + grow] =
+          -INFINITY;
+    return;
+  }
+  bool ok = true;
   for (int j = 0; j < n && ok; ++j) {
     const int b = (NSB == 1) ? 0 : (j & 1);
     const uint32_t sph = static_cast<uint32_t>(NSB == 1 ? j : (j >> 1)) & 1u;
@@ -488,7 +508,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) tmem_ld_wait(s[ch]);
 
-    const int key0 = j * BN;
+    const int key0 = (t.lo + j) * BN;
     const bool masked = (CAUSAL && key0 + BN - 1 > r0) || (key0 + BN > p.N);
     int lim = BN;  // columns [0, lim) of this tile are visible to this row
     if (masked) {
@@ -549,33 +569,53 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   }
 
   if (!ok) return;
-  // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+  // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with split-KV the
+  // normalised fp32 partial O and the partial LSE go to the workspace.
+  constexpr bool split_mode = SPLIT;
+  const bool valid = grow < p.N;
   ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
   if (!ok) return;
   tc_fence_after_sync();
   const float inv_l = 1.f / l;
-  const bool valid = grow < p.N;
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0)) * D;
+  const size_t row = static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0);
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
+  float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.N + row) * D;
 #pragma unroll
   for (int ch = 0; ch < D / 32; ++ch) {
     uint32_t ov[32];
     tmem_ld_32x32b_x32(o_t + ch * 32, ov);
     tmem_ld_wait(ov);
-    uint32_t pk[16];
+    if constexpr (split_mode) {
+      if (valid) {
+        float4* dst = reinterpret_cast<float4*>(prow + ch * 32);
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
-      pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
-    if (valid) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+        for (int v4 = 0; v4 < 8; ++v4)
+          dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
+                                __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
+      }
+    } else {
+      uint32_t pk[16];
 #pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4)
-        dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+      }
     }
   }
-  if (valid) p.lse[static_cast<size_t>(t.bh) * p.N + grow] = (m_used + __log2f(l)) * kLn2;
+  if (valid) {
+    const float lse = (m_used + __log2f(l)) * kLn2;
+    if constexpr (split_mode)
+      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.N + row] = lse;
+    else
+      p.lse[row] = lse;
+  }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -585,7 +625,7 @@ __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Tile<D, CAUSAL> t = make_tile<D, CAUSAL>(p);
+  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT>(p);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
   const Waiter w{abort_flag, p.status};
@@ -618,16 +658,16 @@ __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
   // split differs per path), then meets the others at the teardown barrier.
   if (warp < 4 * L::NQ) {
     if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
-    softmax_role<D, CAUSAL>(warp >> 2, tmem, sbase, t, p, w);
+    softmax_role<D, CAUSAL, SPLIT>(warp >> 2, tmem, sbase, t, p, w);
     tc_fence_before_sync();
     __syncthreads();
   } else {
     if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
     if (warp == L::TMA_WARP) {
-      if (lane == 0) producer_role<D, CAUSAL>(&tm_q, &tm_k, &tm_v, sbase, t, w);
+      if (lane == 0) producer_role<D, CAUSAL, SPLIT>(&tm_q, &tm_k, &tm_v, sbase, t, w);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
-      mma_role<D, CAUSAL>(tmem, sbase, t, w);
+      mma_role<D, CAUSAL, SPLIT>(tmem, sbase, t, w);
       __syncwarp();
     }
     tc_fence_before_sync();

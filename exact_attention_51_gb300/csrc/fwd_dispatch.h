@@ -14,14 +14,25 @@ struct FwdParams {
   int BH;
   int n_qblk;            // CTAs per head
   float scale_log2;      // scale * log2(e)
+  // Split-KV: kv_splits CTAs share the key tiles of one query block; each
+  // writes its normalised partial O (fp32 [kv_splits][BH][N][D]) and its
+  // partial LSE (fp32 [kv_splits][BH][N], -inf when it saw no key) instead of
+  // the final outputs.  kv_splits == 1 writes o / lse directly.
+  int kv_splits;
+  float* o_part;
+  float* lse_part;
 };
 
 struct FwdVariant {
   int kv_rows;         // keys per K/V tile (TMA box rows of K and V)
   int q_rows_per_cta;  // query rows per CTA (multiple of the 128-row Q box)
   cudaError_t (*launch)(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                        const FwdParams& p, bool causal, cudaStream_t stream);
+                        const FwdParams& p, bool causal, cudaStream_t stream);  // grid covers kv_splits
 };
+
+// Merges kv_splits partial results per row into bf16 O and fp32 LSE.
+cudaError_t launch_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse,
+                           long long rows, int kv_splits, cudaStream_t stream);
 
 FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();

@@ -7,11 +7,11 @@
 
 namespace ea51 {
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const FwdParams& p, cudaStream_t stream) {
   using L = Layout<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT>;
   // The dynamic shared-memory opt-in is per device; remember which are done.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -23,7 +23,8 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  const unsigned grid = static_cast<unsigned>(p.n_qblk) * static_cast<unsigned>(p.BH);
+  const unsigned grid = static_cast<unsigned>(p.n_qblk) * static_cast<unsigned>(p.BH) *
+                        static_cast<unsigned>(p.kv_splits);
   kern<<<grid, L::THREADS, L::SMEM_ALLOC, stream>>>(*tq, *tk, *tv, p);
   return cudaGetLastError();
 }
@@ -31,8 +32,13 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
 template <int D>
 cudaError_t launch_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                      const FwdParams& p, bool causal, cudaStream_t stream) {
-  return causal ? launch_one<D, true>(tq, tk, tv, p, stream)
-                : launch_one<D, false>(tq, tk, tv, p, stream);
+  // split-KV partial outputs use their own instantiation, so the single-pass
+  // kernel carries none of that epilogue
+  if (p.kv_splits > 1)
+    return causal ? launch_one<D, true, true>(tq, tk, tv, p, stream)
+                  : launch_one<D, false, true>(tq, tk, tv, p, stream);
+  return causal ? launch_one<D, true, false>(tq, tk, tv, p, stream)
+                : launch_one<D, false, false>(tq, tk, tv, p, stream);
 }
 
 template <int D>

@@ -63,6 +63,9 @@ WORKLOADS = {
     "dsweep64": Workload("dsweep64", 4, 16, 8192, 64, (False, True), "uniform", 5000),
     "dsweep128": Workload("dsweep128", 4, 16, 8192, 128, (False, True), "uniform", 5100),
     "dsweep256": Workload("dsweep256", 4, 16, 8192, 256, (False, True), "uniform", 5200),
+    # not one of the five workload families: a narrow launch (B*H*N/256 = 128
+    # query blocks < the SM count) where split-KV is meant to help
+    "narrow": Workload("narrow", 1, 4, 8192, 128, (False, True), "normal", 6000),
 }
 
 

@@ -41,6 +41,8 @@
 #ifndef EXACT_ATTENTION_51_GB300_ATTN_FWD_H
 #define EXACT_ATTENTION_51_GB300_ATTN_FWD_H
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define ATTN_API __attribute__((visibility("default")))
 #else
@@ -92,6 +94,42 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  */
 ATTN_API int attn_fwd_check_args(const void* q, const void* k, const void* v, const void* o,
                         const float* lse, int B, int H, int N, int d, float scale, int causal);
+
+/*
+ * Split-KV variant of attn_fwd.  The key tiles of each 128..256-row query
+ * block are shared out over `num_splits` thread blocks, which raises the
+ * number of blocks in flight when B*H*N is too small to fill the GPU; each
+ * block writes a normalised fp32 partial output and its partial
+ * log-sum-exp to `workspace`, and a second kernel on the same stream merges
+ * them per row (L = ln sum_s exp(L_s), O = sum_s exp(L_s - L) O_s -- the
+ * associative merge of softmax states the online-softmax trick rests on,
+ * "Tri Dao: prediction"; the "algebraic aggregates" of HN item 40939030).
+ * The result equals attn_fwd's up to rounding.
+ *
+ *   num_splits  1..64.  1 runs attn_fwd itself (workspace unused, may be
+ *               NULL).
+ *   workspace   device buffer of at least
+ *               attn_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+ *               bytes, 256-byte aligned, owned by the caller, not
+ *               overlapping q, k, v, o or lse.  Its contents on entry do not
+ *               matter; it is scratch until the merge kernel has run.
+ *   other arguments and errors as attn_fwd; a missing, short or misplaced
+ *   workspace or num_splits out of range is ATTN_ERR_INVALID_ARG /
+ *   ATTN_ERR_MISALIGNED / ATTN_ERR_ALIAS.  Enqueues two kernels.
+ */
+ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int N, int d, float scale, int causal, int num_splits,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1 or invalid
+ * sizes): num_splits * B*H*N * (d + 1) * 4 bytes, each part 256-byte padded.
+ * Host-only. */
+ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/* A split count for attn_fwd_splitkv: 1 when B*H query blocks already fill
+ * `num_sms` multiprocessors, else enough splits for about one wave while
+ * every share keeps at least four key tiles.  Host-only. */
+ATTN_API int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms);
 
 /* Static, NUL-terminated English text for a status code. */
 ATTN_API const char* attn_status_string(int status);

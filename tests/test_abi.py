@@ -124,3 +124,50 @@ def test_python_binding_rejects_cpu_tensors(lib):
     x = torch.zeros((1, 1, 4, 64), dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         ea.attn_fwd(x, x, x)
+
+
+# ------------------------------------------------------------------ split-KV
+
+def test_splitkv_workspace_size(lib):
+    def align(x):
+        return (x + 255) // 256 * 256
+    for (B, H, N, d, S) in [(1, 2, 128, 64, 2), (2, 3, 1000, 128, 5), (1, 1, 7, 256, 64)]:
+        rows = B * H * N
+        want = align(S * rows * d * 4) + align(S * rows * 4)
+        assert ea.attn_fwd_splitkv_workspace_size(B, H, N, d, S) == want
+    assert ea.attn_fwd_splitkv_workspace_size(1, 1, 128, 64, 1) == 0
+    for bad in [(0, 1, 128, 64, 2), (1, 1, 128, 96, 2), (1, 1, 128, 64, 0), (1, 1, 128, 64, 65)]:
+        assert ea.attn_fwd_splitkv_workspace_size(*bad) == 0
+
+
+def test_splitkv_split_heuristic(lib):
+    # a launch that already fills the GPU is not split
+    assert ea.attn_fwd_splitkv_num_splits(4, 16, 4096, 128, True, 152) == 1
+    # one head of 8192 keys: 32 CTAs of 256 rows -> about 5 splits
+    s = ea.attn_fwd_splitkv_num_splits(1, 1, 8192, 128, False, 152)
+    assert 2 <= s <= 64 and s * 32 >= 152
+    # every share keeps >= 4 key tiles
+    assert ea.attn_fwd_splitkv_num_splits(1, 1, 512, 128, False, 152) == 1
+    assert ea.attn_fwd_splitkv_num_splits(1, 1, 1024, 64, False, 152) == 2
+    assert ea.attn_fwd_splitkv_num_splits(1, 1, 1024, 64, False, 0) == 1
+
+
+def _splitkv(lib, p, splits, ws, ws_bytes, **kw):
+    B, H, N, d = kw.get("B", 1), kw.get("H", 2), kw.get("N", 128), kw.get("d", 64)
+    return lib.attn_fwd_splitkv(*p, B, H, N, d, 0.125, 0, splits, ws, ws_bytes, None)
+
+
+def test_splitkv_rejects_bad_arguments(lib):
+    n = 1 * 2 * 128 * 64 * 2
+    p = ptrs(n)
+    need = ea.attn_fwd_splitkv_workspace_size(1, 2, 128, 64, 4)
+    ws = A + (1 << 30)
+    assert _splitkv(lib, p, 0, ws, need) == ea.ATTN_ERR_INVALID_ARG
+    assert _splitkv(lib, p, 65, ws, need) == ea.ATTN_ERR_INVALID_ARG
+    assert _splitkv(lib, p, 4, None, need) == ea.ATTN_ERR_INVALID_ARG
+    assert _splitkv(lib, p, 4, ws, need - 1) == ea.ATTN_ERR_INVALID_ARG
+    assert _splitkv(lib, p, 4, ws + 16, need) == ea.ATTN_ERR_MISALIGNED
+    assert _splitkv(lib, p, 4, p[1] - (p[1] % 256), need) == ea.ATTN_ERR_ALIAS  # over k
+    q = list(p)
+    q[0] = 0
+    assert _splitkv(lib, q, 4, ws, need) == ea.ATTN_ERR_INVALID_ARG
