@@ -5,9 +5,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <functional>
 #include <mutex>
+#include <vector>
 
 #include "attn_fwd.h"
 #include "fwd_dispatch.h"
@@ -225,16 +228,47 @@ size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_split
 int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1) return 1;
   const ea51::FwdVariant var = variant_for(d);
-  const int64_t ctas = static_cast<int64_t>(B) * H * ((N + var.q_rows_per_cta - 1) / var.q_rows_per_cta);
-  const int64_t key_tiles = (static_cast<int64_t>(N) + var.kv_rows - 1) / var.kv_rows;
-  // Split only while the launch fills less than one wave, keeping at least
-  // four key tiles per share (causal blocks see about half the keys).
-  if (ctas >= num_sms) return 1;
-  int64_t s = (num_sms + ctas - 1) / ctas;
-  const int64_t max_by_tiles = (causal ? key_tiles / 2 : key_tiles) / 4;
-  if (s > max_by_tiles) s = max_by_tiles;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return s < 1 ? 1 : static_cast<int>(s);
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t nq = (static_cast<int64_t>(N) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  const int64_t ctas = BH * nq;
+  if (ctas >= num_sms) return 1;  // a full wave already: splitting only adds the merge
+  // Model: a CTA costs (key tiles it visits + 2) time units, CTAs start in
+  // launch order (heaviest first) on the least-loaded multiprocessor, and a
+  // split launch pays 5 % for the merge kernel and the workspace traffic.
+  // Pick the split count with the smallest modelled makespan.
+  std::vector<int64_t> work;
+  std::vector<int64_t> sm;
+  double best = 0;
+  int best_s = 1;
+  for (int s = 1; s <= 16 && s <= kMaxSplits; ++s) {
+    work.clear();
+    for (int64_t qb = 0; qb < nq; ++qb) {
+      const int64_t last_row = std::min<int64_t>((qb + 1) * var.q_rows_per_cta, N) - 1;
+      const int64_t tiles = causal ? last_row / var.kv_rows + 1
+                                   : (static_cast<int64_t>(N) + var.kv_rows - 1) / var.kv_rows;
+      const int64_t share = (tiles + s - 1) / s;
+      for (int i = 0; i < s; ++i) {
+        const int64_t t = std::min<int64_t>(share, tiles - i * share);
+        for (int64_t h = 0; h < BH; ++h) work.push_back(std::max<int64_t>(t, 0) + 2);
+      }
+    }
+    std::sort(work.begin(), work.end(), std::greater<int64_t>());
+    sm.assign(static_cast<size_t>(num_sms), 0);
+    std::make_heap(sm.begin(), sm.end(), std::greater<int64_t>());
+    int64_t makespan = 0;
+    for (const int64_t wk : work) {
+      std::pop_heap(sm.begin(), sm.end(), std::greater<int64_t>());
+      sm.back() += wk;
+      makespan = std::max(makespan, sm.back());
+      std::push_heap(sm.begin(), sm.end(), std::greater<int64_t>());
+    }
+    const double cost = static_cast<double>(makespan) * (s > 1 ? 1.05 : 1.0);
+    if (s == 1 || cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  return best_s;
 }
 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -126,9 +126,12 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
  * Host-only. */
 ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
-/* A split count for attn_fwd_splitkv: 1 when B*H query blocks already fill
- * `num_sms` multiprocessors, else enough splits for about one wave while
- * every share keeps at least four key tiles.  Host-only. */
+/* A split count (1..16) for attn_fwd_splitkv on a GPU with `num_sms`
+ * multiprocessors: 1 when the B*H query blocks already fill one wave;
+ * otherwise the count with the shortest modelled run time (blocks cost
+ * their key tiles plus a fixed overhead and start heaviest first on the
+ * least-loaded multiprocessor; a split run pays 5 % for the merge).
+ * Host-only. */
 ATTN_API int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms);
 
 /* Static, NUL-terminated English text for a status code. */

@@ -141,15 +141,21 @@ def test_splitkv_workspace_size(lib):
 
 
 def test_splitkv_split_heuristic(lib):
+    f = ea.attn_fwd_splitkv_num_splits
     # a launch that already fills the GPU is not split
-    assert ea.attn_fwd_splitkv_num_splits(4, 16, 4096, 128, True, 152) == 1
-    # one head of 8192 keys: 32 CTAs of 256 rows -> about 5 splits
-    s = ea.attn_fwd_splitkv_num_splits(1, 1, 8192, 128, False, 152)
-    assert 2 <= s <= 64 and s * 32 >= 152
-    # every share keeps >= 4 key tiles
-    assert ea.attn_fwd_splitkv_num_splits(1, 1, 512, 128, False, 152) == 1
-    assert ea.attn_fwd_splitkv_num_splits(1, 1, 1024, 64, False, 152) == 2
-    assert ea.attn_fwd_splitkv_num_splits(1, 1, 1024, 64, False, 0) == 1
+    assert f(4, 16, 4096, 128, True, 152) == 1
+    assert f(1, 32, 16384, 128, True, 152) == 1
+    # one head of 8192 keys (32 query blocks of 256 rows): split
+    assert 2 <= f(1, 1, 8192, 128, False, 152) <= 16
+    # 128 equal blocks already use 84 % of 152 SMs: splitting does not pay
+    assert f(1, 4, 8192, 128, False, 152) == 1
+    # the same shape causal: the heavy diagonal blocks bound the run, split
+    assert f(1, 4, 8192, 128, True, 152) >= 2
+    # degenerate inputs
+    assert f(1, 1, 1024, 64, False, 0) == 1
+    assert f(0, 1, 1024, 64, False, 152) == 1
+    for args in [(1, 1, 1, 64, False), (1, 2, 100000, 256, True), (2, 3, 777, 128, True)]:
+        assert 1 <= f(*args, 152) <= 16
 
 
 def _splitkv(lib, p, splits, ws, ws_bytes, **kw):
