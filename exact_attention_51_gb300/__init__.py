@@ -32,6 +32,8 @@ ATTN_ERR_ALIAS = 3
 ATTN_ERR_UNSUPPORTED_DEVICE = 4
 ATTN_ERR_LAUNCH = 5
 ATTN_ERR_TIMEOUT = 6
+ATTN_ERR_NOALLOC_TOO_LARGE = 7
+NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024  # ATTN_NOALLOC_WORKSPACE_BYTES
 
 SUPPORTED_HEAD_DIMS = (64, 128, 256)
 
@@ -79,6 +81,9 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_splitkv_workspace_size.restype = ctypes.c_size_t
         lib.attn_fwd_splitkv_num_splits.argtypes = [_int, _int, _int, _int, _int, _int]
         lib.attn_fwd_splitkv_num_splits.restype = _int
+        lib.attn_fwd_splitkv_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int,
+                                                 _flt, _int, _int, _vp]
+        lib.attn_fwd_splitkv_noalloc.restype = _int
         _lib = lib
         return lib
 
@@ -171,6 +176,28 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                                   _stream_handle(stream, q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None = None,
+                             num_splits: int = 2, out=None, lse=None, stream=None):
+    """``attn_fwd_splitkv`` whose workspace is the library's fixed device
+    array (NOALLOC_WORKSPACE_BYTES): the C call allocates nothing, for
+    callers that cannot allocate device memory.  Calls that overlap on the
+    GPU race on the shared array; ``out`` / ``lse`` are allocated here with
+    torch unless given."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    with torch.cuda.device(q.device):
+        rc = load_library().attn_fwd_splitkv_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), int(num_splits), _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv_noalloc")
     return out, lse
 
 

@@ -304,6 +304,8 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
     case ATTN_ERR_LAUNCH: return "CUDA call failed (see attn_last_cuda_error)";
     case ATTN_ERR_TIMEOUT: return "a device-side wait timed out; outputs are invalid";
+    case ATTN_ERR_NOALLOC_TOO_LARGE:
+      return "problem needs more split-KV workspace than the fixed no-allocation buffer holds";
     default: return "unknown status";
   }
 }

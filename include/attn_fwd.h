@@ -63,8 +63,13 @@ enum attn_status {
   ATTN_ERR_ALIAS = 3,              /* o or lse overlaps an input, or lse overlaps o */
   ATTN_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
   ATTN_ERR_LAUNCH = 5,             /* CUDA runtime/driver call failed; see attn_last_cuda_error */
-  ATTN_ERR_TIMEOUT = 6             /* a device-side wait gave up (see attn_fwd_device_status) */
+  ATTN_ERR_TIMEOUT = 6,            /* a device-side wait gave up (see attn_fwd_device_status) */
+  ATTN_ERR_NOALLOC_TOO_LARGE = 7   /* attn_fwd_splitkv_noalloc: the problem needs more
+                                      workspace than ATTN_NOALLOC_WORKSPACE_BYTES */
 };
+
+/* Size of the fixed device workspace behind attn_fwd_splitkv_noalloc. */
+#define ATTN_NOALLOC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 
 /*
  * Fused exact attention forward.
@@ -133,6 +138,36 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int 
  * least-loaded multiprocessor; a split run pays 5 % for the merge).
  * Host-only. */
 ATTN_API int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms);
+
+/*
+ * attn_fwd_splitkv without a caller-provided workspace.  The pages have no
+ * counterpart of this entry point; it exists for callers that cannot
+ * allocate device memory: a plugin whose host framework hands it only the
+ * input and output buffers, or a serving loop that must keep cudaMalloc off
+ * its hot path (cudaMalloc can synchronise the whole device, and where a
+ * pool allocator owns the memory it can fail or fragment it).
+ *
+ * The split-KV workspace is a fixed array of ATTN_NOALLOC_WORKSPACE_BYTES
+ * (64 MiB) of device memory inside the library.  Every device the library is
+ * used on holds it from first use until the process exits.  The call
+ * allocates nothing itself.
+ *
+ *   Arguments, results and errors as attn_fwd_splitkv (num_splits 1 needs
+ *   no workspace and runs attn_fwd).  A problem whose workspace
+ *   (attn_fwd_splitkv_workspace_size) exceeds ATTN_NOALLOC_WORKSPACE_BYTES
+ *   is rejected with ATTN_ERR_NOALLOC_TOO_LARGE before anything is launched.
+ *   The first call on a device looks up the array's device address with the
+ *   CUDA runtime (a one-time set-up per device, made with that device
+ *   current); make that first call before any stream capture.
+ *   All calls share the one array, and it keeps what the last call left in
+ *   it.  Nothing in it has to start at zero: each call writes every value it
+ *   later reads.  Calls whose kernels overlap on the GPU (several streams,
+ *   several host threads) race on the array and give wrong results: order
+ *   them, for instance on one stream.
+ */
+ATTN_API int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int H, int N, int d, float scale,
+                                      int causal, int num_splits, void* stream);
 
 /* Static, NUL-terminated English text for a status code. */
 ATTN_API const char* attn_status_string(int status);
