@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_splitkv_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int,
                                                  _flt, _int, _int, _vp]
         lib.attn_fwd_splitkv_noalloc.restype = _int
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+        lib.attn_selftest_wait_timeout.restype = _int
         _lib = lib
         return lib
 
@@ -241,6 +243,15 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_selftest_wait_timeout(timeout_ms: int = 100, stream=None, device=None) -> int:
+    """Enqueue the bounded-wait self-test kernel (see include/attn_fwd.h)."""
+    import torch
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(device):
+        return int(load_library().attn_selftest_wait_timeout(int(timeout_ms),
+                                                             _stream_handle(stream, device)))
 
 
 def attn_fwd_device_status(stream=None, device=None):

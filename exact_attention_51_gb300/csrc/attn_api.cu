@@ -129,6 +129,13 @@ int encode_map(CUtensorMap* map, const void* base, int64_t BH, int N, int d, int
 
 }  // namespace
 
+namespace ea51 {
+unsigned int* status_word() {
+  DeviceState* ds = nullptr;
+  return device_state(&ds) == ATTN_OK ? ds->status : nullptr;
+}
+}  // namespace ea51
+
 extern "C" {
 
 int attn_fwd_check_args(const void* q, const void* k, const void* v, const void* o,
@@ -327,5 +334,17 @@ int attn_fwd_device_status(void* stream, unsigned int* detail) {
 }
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_selftest_wait_timeout(unsigned int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return ATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return rc;
+  const cudaError_t e = ea51::launch_wait_selftest(
+      ds->status, static_cast<unsigned long long>(timeout_ms) * 1000000ull,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
+}
 
 }  // extern "C"

@@ -121,7 +121,8 @@ struct Waiter {
 };
 
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Waiter w, uint32_t code,
-                                       bool honour_abort) {
+                                       bool honour_abort,
+                                       unsigned long long timeout_ns = kWaitTimeoutNs) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
@@ -133,7 +134,7 @@ static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, 
         return false;
       }
     }
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (global_timer_ns() - t0 > timeout_ns) {
       atomicCAS(w.status, 0u, code);
       *w.abort_flag = 1u;
       return false;
@@ -169,6 +170,7 @@ enum : uint32_t {
   kCodeSoftO = 0x122,
   kCodeSoftFinal = 0x123,
   kCodeDrain = 0x131,
+  kCodeSelfTest = 0x1f1,
 };
 
 // ---------------------------------------------------------------- roles

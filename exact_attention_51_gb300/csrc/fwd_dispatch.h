@@ -34,6 +34,15 @@ struct FwdVariant {
 cudaError_t launch_combine(int d, const float* o_part, const float* lse_part, void* o, float* lse,
                            long long rows, int kv_splits, cudaStream_t stream);
 
+// Device address of the current device's wait-timeout status word (set up by
+// the C ABI's per-device initialisation; nullptr if that failed).
+unsigned int* status_word();
+
+// Launches a one-block kernel that waits on an mbarrier nothing arrives on,
+// with the kernel's bounded wait cut to `timeout_ns`.
+cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long timeout_ns,
+                                 cudaStream_t stream);
+
 FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();
 FwdVariant fwd_variant_d256();

@@ -188,6 +188,17 @@ ATTN_API int attn_fwd_device_status(void* stream, unsigned int* detail);
  * inside the library (0 if none). */
 ATTN_API int attn_last_cuda_error(void);
 
+/*
+ * Self-test of the bounded waits behind attn_fwd_device_status: enqueues one
+ * small kernel whose single wait (on an mbarrier nothing arrives on) gives up
+ * after `timeout_ms` (1..10000) milliseconds, records its code (0x1f1) in the
+ * device status word and exits.  A following attn_fwd_device_status returns
+ * ATTN_ERR_TIMEOUT with that code and clears the word; the CUDA context stays
+ * usable.  The status word is shared with every attn_fwd launch on the
+ * device, so run this only when no other launch of the library is in flight.
+ */
+ATTN_API int attn_selftest_wait_timeout(unsigned int timeout_ms, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
