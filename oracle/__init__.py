@@ -64,6 +64,15 @@ def _bind(lib):
     lib.attn_ref_bf16_rows.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _dbl,
                                        ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
     lib.attn_ref_bf16_rows.restype = ctypes.c_int
+    lib.attn_ref_f64_qk.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                    _dbl, ctypes.c_int, ctypes.c_int]
+    lib.attn_ref_f64_qk.restype = ctypes.c_int
+    lib.attn_ref_bf16_qk.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                     _dbl, ctypes.c_int, ctypes.c_int]
+    lib.attn_ref_bf16_qk.restype = ctypes.c_int
+    lib.attn_ref_bf16_qk_rows.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _dbl,
+                                          ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+    lib.attn_ref_bf16_qk_rows.restype = ctypes.c_int
     lib.attn_ref_max_threads.argtypes = []
     lib.attn_ref_max_threads.restype = ctypes.c_int
     return lib
@@ -156,6 +165,58 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle attn_ref_bf16_rows failed: {rc}")
         return o[:R], lse[:R]
+
+
+    # -- a key length of its own: q [B,H,Nq,d], k / v [B,H,Nk,d]; causal
+    # -- means key j visible to query i iff j <= i + Nk - Nq (needs Nk >= Nq)
+
+    def attn_f64_qk(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
+        q, k, v = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v))
+        B, H, Nq, Nk, d = _qk_shapes(q, k, v)
+        o = np.empty((B, H, Nq, d), np.float64)
+        lse = np.empty((B, H, Nq), np.float64)
+        rc = self.lib.attn_ref_f64_qk(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data,
+                                      lse.ctypes.data, B, H, Nq, Nk, d, float(scale),
+                                      int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_f64_qk failed: {rc}")
+        return o, lse
+
+    def attn_bf16_qk(self, q, k, v, causal: bool, scale: float, nthreads: int = 0):
+        qb, kb, vb = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        B, H, Nq, Nk, d = _qk_shapes(qb, kb, vb)
+        o = np.empty((B, H, Nq, d), np.float64)
+        lse = np.empty((B, H, Nq), np.float64)
+        rc = self.lib.attn_ref_bf16_qk(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
+                                       o.ctypes.data, lse.ctypes.data, B, H, Nq, Nk, d,
+                                       float(scale), int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_bf16_qk failed: {rc}")
+        return o, lse
+
+    def attn_bf16_qk_rows(self, q, k, v, causal: bool, scale: float, rows, nthreads: int = 0):
+        qb, kb, vb = _as_bf16_bits(q), _as_bf16_bits(k), _as_bf16_bits(v)
+        B, H, Nq, Nk, d = _qk_shapes(qb, kb, vb)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        R = rows.shape[0]
+        o = np.empty((max(R, 1), d), np.float64)
+        lse = np.empty((max(R, 1),), np.float64)
+        rc = self.lib.attn_ref_bf16_qk_rows(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data, B, H,
+                                            Nq, Nk, d, float(scale), int(bool(causal)),
+                                            rows.ctypes.data, R, o.ctypes.data, lse.ctypes.data,
+                                            int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_bf16_qk_rows failed: {rc}")
+        return o[:R], lse[:R]
+
+
+def _qk_shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("expected [B,H,Nq,d] queries and [B,H,Nk,d] keys / values")
+    B, H, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k, v must be [B,H,Nk,d] with q's B, H and d")
+    return B, H, Nq, k.shape[2], d
 
 
 def default() -> Oracle:

@@ -14,9 +14,11 @@
  *   o_ic  = sum_j exp(s_ij - m_i) v_jc / l_i            (pass 3)
  *   lse_i = m_i + ln l_i
  *
- * "visible j" is every key 0..N-1, or 0..i when causal (the lower
- * "triangular matrix" of the scores; key j is visible to query i iff j <= i,
- * with Nq = Nk = N, so the diagonal is always visible and no row is empty).
+ * "visible j" is every key 0..Nk-1, or 0..i+Nk-Nq when causal (the lower
+ * "triangular matrix" of the scores, aligned to the bottom-right corner when
+ * there are more keys than queries, Nk >= Nq; with Nq = Nk = N key j is
+ * visible to query i iff j <= i).  The diagonal is always visible, so no row
+ * is empty.
  *
  * Sources: "Tri Dao: prediction" (highsignal podcast transcript) -- exact
  * attention whose softmax needs a sum across the row of the attention matrix,
@@ -55,13 +57,14 @@ static double bf16_bits_to_f64(uint16_t h) {
 }
 
 /*
- * One query row against one head's keys and values (all fp64, row-major
- * [N,d]).  `s` is caller-provided scratch of N doubles.
+ * One query row i against one head's keys and values (fp64, row-major
+ * [Nk,d]); `off` = Nk - Nq shifts the causal diagonal.  `s` is caller-provided
+ * scratch of Nk doubles.
  */
 static void attend_row(const double *q_i, const double *K, const double *V,
-                       int64_t N, int64_t d, int64_t i, double scale,
+                       int64_t Nk, int64_t d, int64_t i, int64_t off, double scale,
                        int causal, double *s, double *o_i, double *lse_i) {
-    int64_t last = causal ? i : N - 1; /* visible keys are 0..last */
+    int64_t last = causal ? i + off : Nk - 1; /* visible keys are 0..last */
 
     /* scores */
     for (int64_t j = 0; j <= last; ++j) {
@@ -90,10 +93,12 @@ static void attend_row(const double *q_i, const double *K, const double *V,
     *lse_i = m + log(l);
 }
 
-static int check_sizes(int64_t B, int64_t H, int64_t N, int64_t d) {
-    if (B < 1 || H < 1 || N < 1 || d < 1) return ORACLE_EINVAL;
+static int check_sizes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return ORACLE_EINVAL;
+    if (causal && Nk < Nq) return ORACLE_EINVAL; /* first rows would see no key */
     /* keep B*H*N*d well inside int64 */
-    if ((double)B * (double)H * (double)N * (double)d > 4.0e18) return ORACLE_EINVAL;
+    const double n = (double)(Nq > Nk ? Nq : Nk);
+    if ((double)B * (double)H * n * (double)d > 4.0e18) return ORACLE_EINVAL;
     return ORACLE_OK;
 }
 
@@ -106,18 +111,18 @@ static void set_threads(int nthreads) {
 }
 
 /*
- * Rows of one head: `rows` lists query indices i (0..N-1) of head (b,h);
+ * Rows of one head: `rows` lists query indices i (0..Nq-1) of head (b,h);
  * outputs go to o_out[r*d..] and lse_out[r] for the r-th listed row.
- * K, V (and Q rows) are fp64 [N,d] of that head.
+ * Q rows are fp64 [Nq,d], K and V fp64 [Nk,d] of that head.
  */
 static int head_rows(const double *Qh, const double *Kh, const double *Vh,
-                     int64_t N, int64_t d, double scale, int causal,
+                     int64_t Nq, int64_t Nk, int64_t d, double scale, int causal,
                      const int64_t *rows, int64_t nrows, double *o_out,
                      double *lse_out) {
     int err = 0;
 #pragma omp parallel
     {
-        double *s = (double *)malloc((size_t)N * sizeof(double));
+        double *s = (double *)malloc((size_t)Nk * sizeof(double));
         if (!s) {
 #pragma omp atomic write
             err = 1;
@@ -126,7 +131,7 @@ static int head_rows(const double *Qh, const double *Kh, const double *Vh,
         for (int64_t r = 0; r < nrows; ++r) {
             if (!s) continue;
             const int64_t i = rows ? rows[r] : r;
-            attend_row(Qh + i * d, Kh, Vh, N, d, i, scale, causal, s,
+            attend_row(Qh + i * d, Kh, Vh, Nk, d, i, Nk - Nq, scale, causal, s,
                        o_out + r * d, lse_out + r);
         }
         free(s);
@@ -136,21 +141,27 @@ static int head_rows(const double *Qh, const double *Kh, const double *Vh,
 
 /* ---------------------------------------------------------------- fp64 in */
 
-/* Whole tensors, fp64 inputs. */
-int attn_ref_f64(const double *q, const double *k, const double *v, double *o,
-                 double *lse, int64_t B, int64_t H, int64_t N, int64_t d,
-                 double scale, int causal, int nthreads) {
+/* Whole tensors, fp64 inputs: q, o [B,H,Nq,d], k, v [B,H,Nk,d], lse [B,H,Nq]. */
+int attn_ref_f64_qk(const double *q, const double *k, const double *v, double *o,
+                    double *lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                    int64_t d, double scale, int causal, int nthreads) {
     if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
-    int rc = check_sizes(B, H, N, d);
+    int rc = check_sizes(B, H, Nq, Nk, d, causal);
     if (rc) return rc;
     set_threads(nthreads);
     for (int64_t bh = 0; bh < B * H; ++bh) {
-        const int64_t off = bh * N * d;
-        rc = head_rows(q + off, k + off, v + off, N, d, scale, causal, NULL, N,
-                       o + off, lse + bh * N);
+        rc = head_rows(q + bh * Nq * d, k + bh * Nk * d, v + bh * Nk * d, Nq, Nk, d,
+                       scale, causal, NULL, Nq, o + bh * Nq * d, lse + bh * Nq);
         if (rc) return rc;
     }
     return ORACLE_OK;
+}
+
+/* Whole tensors, fp64 inputs, Nq = Nk = N. */
+int attn_ref_f64(const double *q, const double *k, const double *v, double *o,
+                 double *lse, int64_t B, int64_t H, int64_t N, int64_t d,
+                 double scale, int causal, int nthreads) {
+    return attn_ref_f64_qk(q, k, v, o, lse, B, H, N, N, d, scale, causal, nthreads);
 }
 
 /* ---------------------------------------------------------------- bf16 in */
@@ -161,27 +172,27 @@ static void decode_head(const uint16_t *src, double *dst, int64_t n) {
 }
 
 /*
- * Selected rows, bf16 inputs.  rows[r] is a flat row id (b*H + h)*N + i and
- * may come in any order; the r-th result goes to o_rows[r*d..] and
- * lse_rows[r].  Each head that owns at least one listed row is decoded to
- * fp64 once per call.
+ * Selected rows, bf16 inputs: q [B,H,Nq,d], k, v [B,H,Nk,d].  rows[r] is a
+ * flat query-row id (b*H + h)*Nq + i and may come in any order; the r-th
+ * result goes to o_rows[r*d..] and lse_rows[r].  Each head that owns at least
+ * one listed row is decoded to fp64 once per call.
  */
-int attn_ref_bf16_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                       int64_t B, int64_t H, int64_t N, int64_t d, double scale,
-                       int causal, const int64_t *rows, int64_t nrows,
-                       double *o_rows, double *lse_rows, int nthreads) {
+int attn_ref_bf16_qk_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                          double scale, int causal, const int64_t *rows, int64_t nrows,
+                          double *o_rows, double *lse_rows, int nthreads) {
     if (!q || !k || !v || !rows || !o_rows || !lse_rows || nrows < 0)
         return ORACLE_EINVAL;
-    int rc = check_sizes(B, H, N, d);
+    int rc = check_sizes(B, H, Nq, Nk, d, causal);
     if (rc) return rc;
     for (int64_t r = 0; r < nrows; ++r)
-        if (rows[r] < 0 || rows[r] >= B * H * N) return ORACLE_EINVAL;
+        if (rows[r] < 0 || rows[r] >= B * H * Nq) return ORACLE_EINVAL;
     set_threads(nthreads);
 
-    const size_t head_elems = (size_t)N * (size_t)d;
-    double *Qh = (double *)malloc(head_elems * sizeof(double));
-    double *Kh = (double *)malloc(head_elems * sizeof(double));
-    double *Vh = (double *)malloc(head_elems * sizeof(double));
+    const size_t q_elems = (size_t)Nq * (size_t)d, kv_elems = (size_t)Nk * (size_t)d;
+    double *Qh = (double *)malloc(q_elems * sizeof(double));
+    double *Kh = (double *)malloc(kv_elems * sizeof(double));
+    double *Vh = (double *)malloc(kv_elems * sizeof(double));
     int64_t *sel = (int64_t *)malloc((size_t)(nrows ? nrows : 1) * sizeof(int64_t));
     int64_t *pos = (int64_t *)malloc((size_t)(nrows ? nrows : 1) * sizeof(int64_t));
     double *o_tmp = (double *)malloc((size_t)(nrows ? nrows : 1) * (size_t)d * sizeof(double));
@@ -193,17 +204,16 @@ int attn_ref_bf16_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
         int64_t cnt = 0;
         for (int64_t r = 0; r < nrows; ++r)
-            if (rows[r] / N == bh) {
-                sel[cnt] = rows[r] % N;
+            if (rows[r] / Nq == bh) {
+                sel[cnt] = rows[r] % Nq;
                 pos[cnt] = r;
                 ++cnt;
             }
         if (cnt == 0) continue;
-        const int64_t off = bh * (int64_t)head_elems;
-        decode_head(q + off, Qh, (int64_t)head_elems);
-        decode_head(k + off, Kh, (int64_t)head_elems);
-        decode_head(v + off, Vh, (int64_t)head_elems);
-        rc = head_rows(Qh, Kh, Vh, N, d, scale, causal, sel, cnt, o_tmp, l_tmp);
+        decode_head(q + bh * (int64_t)q_elems, Qh, (int64_t)q_elems);
+        decode_head(k + bh * (int64_t)kv_elems, Kh, (int64_t)kv_elems);
+        decode_head(v + bh * (int64_t)kv_elems, Vh, (int64_t)kv_elems);
+        rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, sel, cnt, o_tmp, l_tmp);
         for (int64_t t = 0; t < cnt && rc == ORACLE_OK; ++t) {
             memcpy(o_rows + pos[t] * d, o_tmp + t * d, (size_t)d * sizeof(double));
             lse_rows[pos[t]] = l_tmp[t];
@@ -214,32 +224,47 @@ done:
     return rc;
 }
 
-/* Whole tensors, bf16 inputs. */
-int attn_ref_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  double *o, double *lse, int64_t B, int64_t H, int64_t N,
-                  int64_t d, double scale, int causal, int nthreads) {
+/* Selected rows, bf16 inputs, Nq = Nk = N. */
+int attn_ref_bf16_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       int64_t B, int64_t H, int64_t N, int64_t d, double scale,
+                       int causal, const int64_t *rows, int64_t nrows,
+                       double *o_rows, double *lse_rows, int nthreads) {
+    return attn_ref_bf16_qk_rows(q, k, v, B, H, N, N, d, scale, causal, rows, nrows,
+                                 o_rows, lse_rows, nthreads);
+}
+
+/* Whole tensors, bf16 inputs: q, o [B,H,Nq,d], k, v [B,H,Nk,d], lse [B,H,Nq]. */
+int attn_ref_bf16_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     double *o, double *lse, int64_t B, int64_t H, int64_t Nq,
+                     int64_t Nk, int64_t d, double scale, int causal, int nthreads) {
     if (!q || !k || !v || !o || !lse) return ORACLE_EINVAL;
-    int rc = check_sizes(B, H, N, d);
+    int rc = check_sizes(B, H, Nq, Nk, d, causal);
     if (rc) return rc;
     set_threads(nthreads);
-    const size_t head_elems = (size_t)N * (size_t)d;
-    double *Qh = (double *)malloc(head_elems * sizeof(double));
-    double *Kh = (double *)malloc(head_elems * sizeof(double));
-    double *Vh = (double *)malloc(head_elems * sizeof(double));
+    const size_t q_elems = (size_t)Nq * (size_t)d, kv_elems = (size_t)Nk * (size_t)d;
+    double *Qh = (double *)malloc(q_elems * sizeof(double));
+    double *Kh = (double *)malloc(kv_elems * sizeof(double));
+    double *Vh = (double *)malloc(kv_elems * sizeof(double));
     if (!Qh || !Kh || !Vh) {
         free(Qh); free(Kh); free(Vh);
         return ORACLE_ENOMEM;
     }
     for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
-        const int64_t off = bh * (int64_t)head_elems;
-        decode_head(q + off, Qh, (int64_t)head_elems);
-        decode_head(k + off, Kh, (int64_t)head_elems);
-        decode_head(v + off, Vh, (int64_t)head_elems);
-        rc = head_rows(Qh, Kh, Vh, N, d, scale, causal, NULL, N, o + off,
-                       lse + bh * N);
+        decode_head(q + bh * (int64_t)q_elems, Qh, (int64_t)q_elems);
+        decode_head(k + bh * (int64_t)kv_elems, Kh, (int64_t)kv_elems);
+        decode_head(v + bh * (int64_t)kv_elems, Vh, (int64_t)kv_elems);
+        rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, NULL, Nq,
+                       o + bh * (int64_t)q_elems, lse + bh * Nq);
     }
     free(Qh); free(Kh); free(Vh);
     return rc;
+}
+
+/* Whole tensors, bf16 inputs, Nq = Nk = N. */
+int attn_ref_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  double *o, double *lse, int64_t B, int64_t H, int64_t N,
+                  int64_t d, double scale, int causal, int nthreads) {
+    return attn_ref_bf16_qk(q, k, v, o, lse, B, H, N, N, d, scale, causal, nthreads);
 }
 
 /* Threads OpenMP will use for a parallel region (1 without OpenMP). */

@@ -348,11 +348,61 @@ def pin_rows_api(orc):
     return fails
 
 
+def pin_bottom_right_suffix(orc):
+    """Causal with Nk > Nq keeps the diagonal at the bottom-right corner: the
+    Nq queries are the last Nq of a causal sequence of length Nk, so their
+    result equals the last Nq rows of the square causal attention."""
+    r = _rng(131)
+    fails = []
+    for (Nq, Nk) in [(1, 9), (5, 17), (16, 16), (7, 64)]:
+        qf, k, v = (r.standard_normal((1, 2, Nk, 6)) for _ in range(3))
+        o_full, lse_full = orc.attn_f64(qf, k, v, True, 0.8)
+        o, lse = orc.attn_f64_qk(qf[:, :, Nk - Nq:], k, v, True, 0.8)
+        fails += _close(f"bottom-right O Nq={Nq} Nk={Nk}", o, o_full[:, :, Nk - Nq:], 0.0)
+        fails += _close(f"bottom-right lse Nq={Nq} Nk={Nk}", lse, lse_full[:, :, Nk - Nq:], 0.0)
+    return fails
+
+
+def pin_rectangular_sdpa(orc):
+    """Non-causal Nq != Nk against torch SDPA (fp64) and scipy logsumexp."""
+    from scipy.special import logsumexp
+    r = _rng(141)
+    fails = []
+    for (Nq, Nk) in [(3, 40), (40, 3), (1, 1), (33, 17)]:
+        q = r.standard_normal((2, 1, Nq, 8))
+        k, v = (r.standard_normal((2, 1, Nk, 8)) for _ in range(2))
+        o, lse = orc.attn_f64_qk(q, k, v, False, 0.35)
+        ot = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), scale=0.35).numpy()
+        fails += _close(f"rect sdpa Nq={Nq} Nk={Nk}", o, ot, 1e-12)
+        lt = logsumexp(0.35 * np.einsum("bhic,bhjc->bhij", q, k), axis=-1)
+        fails += _close(f"rect logsumexp Nq={Nq} Nk={Nk}", lse, lt, 1e-12, 1e-12)
+    return fails
+
+
+def pin_rectangular_bf16_rows(orc):
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn((2, 2, 13, 8), generator=g).to(torch.bfloat16)
+    k, v = (torch.randn((2, 2, 29, 8), generator=g).to(torch.bfloat16) for _ in range(2))
+    fails = []
+    for causal in (False, True):
+        o, lse = orc.attn_bf16_qk(q, k, v, causal, 0.3)
+        o2, lse2 = orc.attn_f64_qk(q.double().numpy(), k.double().numpy(), v.double().numpy(),
+                                   causal, 0.3)
+        fails += _close(f"rect bf16 decode causal={causal}", o, o2, 0.0)
+        rows = [0, 12, 13, 25, 51, 38]
+        orow, lrow = orc.attn_bf16_qk_rows(q, k, v, causal, 0.3, rows)
+        fails += _close(f"rect rows o causal={causal}", orow, o.reshape(-1, 8)[rows], 0.0)
+        fails += _close(f"rect rows lse causal={causal}", lrow, lse.reshape(-1)[rows], 0.0)
+    return fails
+
+
 ALL_PINS = [
     pin_online_softmax_tiling, pin_merge_law, pin_identity_values, pin_constant_values,
     pin_single_key, pin_uniform_queries, pin_zero_scale, pin_permutation,
     pin_causal_future_blind, pin_key_shift, pin_linearity_in_v, pin_library_sdpa,
-    pin_golden, pin_bf16_decode, pin_rows_api,
+    pin_golden, pin_bf16_decode, pin_rows_api, pin_bottom_right_suffix, pin_rectangular_sdpa,
+    pin_rectangular_bf16_rows,
 ]
 
 

@@ -54,11 +54,17 @@ def test_rejects_bad_sizes():
 # (description, exact text in attn_ref.c, replacement)
 MUTANTS = [
     ("causal mask excludes the diagonal",
-     "int64_t last = causal ? i : N - 1;",
-     "int64_t last = causal ? (i > 0 ? i - 1 : 0) : N - 1;"),
+     "int64_t last = causal ? i + off : Nk - 1;",
+     "int64_t last = causal ? (i + off > 0 ? i + off - 1 : 0) : Nk - 1;"),
     ("causal mask off (always full row)",
-     "int64_t last = causal ? i : N - 1;",
-     "int64_t last = N - 1;"),
+     "int64_t last = causal ? i + off : Nk - 1;",
+     "int64_t last = Nk - 1;"),
+    ("causal diagonal top-left aligned when Nk > Nq",
+     "int64_t last = causal ? i + off : Nk - 1;",
+     "int64_t last = causal ? i : Nk - 1;"),
+    ("key rows indexed with the query length",
+     "decode_head(k + bh * (int64_t)kv_elems, Kh, (int64_t)kv_elems);\n        decode_head(v + bh * (int64_t)kv_elems, Vh, (int64_t)kv_elems);\n        rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, NULL, Nq,",
+     "decode_head(k + bh * (int64_t)q_elems, Kh, (int64_t)kv_elems);\n        decode_head(v + bh * (int64_t)q_elems, Vh, (int64_t)kv_elems);\n        rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, NULL, Nq,"),
     ("scale dropped", "s[j] = scale * acc;", "s[j] = acc;"),
     ("scale applied twice", "s[j] = scale * acc;", "s[j] = scale * scale * acc;"),
     ("lse without the max", "*lse_i = m + log(l);", "*lse_i = log(l);"),
