@@ -84,6 +84,11 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_splitkv_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int,
                                                  _flt, _int, _int, _vp]
         lib.attn_fwd_splitkv_noalloc.restype = _int
+        lib.attn_fwd_kvcache.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int,
+                                         _flt, _int, _int, _vp, ctypes.c_size_t, _vp]
+        lib.attn_fwd_kvcache.restype = _int
+        lib.attn_fwd_kvcache_num_splits.argtypes = [_int, _int, _int, _int, _int, _int, _int]
+        lib.attn_fwd_kvcache_num_splits.restype = _int
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.attn_selftest_wait_timeout.restype = _int
         _lib = lib
@@ -178,6 +183,53 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                                   _stream_handle(stream, q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attn_fwd_kvcache_num_splits(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool,
+                                num_sms: int) -> int:
+    return int(load_library().attn_fwd_kvcache_num_splits(B, H, Nq, Nk, d, int(bool(causal)),
+                                                           num_sms))
+
+
+def attn_fwd_kvcache(q, k, v, causal: bool = False, scale: float | None = None,
+                     num_splits: int | None = None, out=None, lse=None, workspace=None,
+                     stream=None):
+    """Attention with q [B,H,Nq,d] and k, v [B,H,Nk,d] (KV-cache shapes).
+
+    Causal aligns the diagonal to the bottom-right corner (query i sees keys
+    j <= i + Nk - Nq; needs Nk >= Nq).  ``num_splits`` None picks one from the
+    shape and the SM count; the split-KV workspace is allocated with torch
+    unless given.  Returns ``(o [B,H,Nq,d] bf16, lse [B,H,Nq] fp32)``.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous and 4-D")
+    B, H, Nq, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H, Nk, d] with q's B, H and d")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = attn_fwd_kvcache_num_splits(B, H, Nq, Nk, d, causal, sms)
+    out, lse = _outputs(q, out, lse)
+    need = attn_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().attn_fwd_kvcache(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq,
+            Nk, d, float(scale), int(bool(causal)), int(num_splits), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_kvcache")
     return out, lse
 
 

@@ -45,27 +45,39 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
-               int H, int N, int d, float scale, int /*causal*/) {
+// Argument checks shared by every entry point: q, o [B,H,Nq,d] bf16; k, v
+// [B,H,Nk,d] bf16; lse [B,H,Nq] fp32.  Causal needs Nk >= Nq (the diagonal
+// sits at the bottom-right corner, so every query row sees a key).
+int check_general(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  int B, int H, int Nq, int Nk, int d, float scale, int causal) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   // Launch limits: B*H heads fit the TMA's 32-bit dimension and the grid's
   // 31-bit x extent (with at least 128 query rows per CTA).
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t ctas = BH * ((static_cast<int64_t>(N) + 127) / 128);
+  const int64_t ctas = BH * ((static_cast<int64_t>(Nq) + 127) / 128);
   if (BH > 0x7fffffffLL || ctas > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
   if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4)) return ATTN_ERR_MISALIGNED;
-  const size_t tensor_bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * d * 2;
-  const size_t lse_bytes = static_cast<size_t>(BH) * static_cast<size_t>(N) * 4;
-  for (const void* in : {q, k, v}) {
-    if (overlaps(o, tensor_bytes, in, tensor_bytes)) return ATTN_ERR_ALIAS;
-    if (overlaps(lse, lse_bytes, in, tensor_bytes)) return ATTN_ERR_ALIAS;
+  const size_t q_bytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * d * 2;
+  const size_t kv_bytes = static_cast<size_t>(BH) * static_cast<size_t>(Nk) * d * 2;
+  const size_t lse_bytes = static_cast<size_t>(BH) * static_cast<size_t>(Nq) * 4;
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {q_bytes, kv_bytes, kv_bytes};
+  for (int i = 0; i < 3; ++i) {
+    if (overlaps(o, q_bytes, ins[i], in_bytes[i])) return ATTN_ERR_ALIAS;
+    if (overlaps(lse, lse_bytes, ins[i], in_bytes[i])) return ATTN_ERR_ALIAS;
   }
-  if (overlaps(lse, lse_bytes, o, tensor_bytes)) return ATTN_ERR_ALIAS;
+  if (overlaps(lse, lse_bytes, o, q_bytes)) return ATTN_ERR_ALIAS;
   return ATTN_OK;
+}
+
+int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+               int H, int N, int d, float scale, int causal) {
+  return check_general(q, k, v, o, lse, B, H, N, N, d, scale, causal);
 }
 
 // Per-device set-up: compute capability check and the status word's address.
@@ -154,23 +166,25 @@ ea51::FwdVariant variant_for(int d) {
 
 // Encodes the TMA maps and launches the fused kernel; with kv_splits > 1 the
 // kernel writes partials to o_part / lse_part.
-int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-               int d, float scale, int causal, int kv_splits, float* o_part, float* lse_part,
-               DeviceState* ds, cudaStream_t stream) {
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, float scale, int causal, int kv_splits, float* o_part,
+               float* lse_part, DeviceState* ds, cudaStream_t stream) {
   const ea51::FwdVariant var = variant_for(d);
   const int64_t BH = static_cast<int64_t>(B) * H;
   alignas(64) CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = encode_map(&tq, q, BH, N, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_map(&tk, k, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
-  if ((rc = encode_map(&tv, v, BH, N, d, var.kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tq, q, BH, Nq, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, Nk, d, var.kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, Nk, d, var.kv_rows)) != ATTN_OK) return rc;
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
   p.status = ds->status;
-  p.N = N;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal_off = Nk - Nq;
   p.BH = static_cast<int>(BH);
-  p.n_qblk = (N + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  p.n_qblk = (Nq + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.kv_splits = kv_splits;
   p.o_part = o_part;
@@ -185,64 +199,70 @@ constexpr int kMaxSplits = 64;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Bytes of split-KV workspace: fp32 partial O, then fp32 partial LSE.
-size_t splitkv_bytes(int64_t BH, int N, int d, int splits, size_t* lse_offset) {
-  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N);
+size_t splitkv_bytes(int64_t BH, int Nq, int d, int splits, size_t* lse_offset) {
+  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(Nq);
   const size_t o_bytes = align256(static_cast<size_t>(splits) * rows * d * 4);
   if (lse_offset) *lse_offset = o_bytes;
   return o_bytes + align256(static_cast<size_t>(splits) * rows * 4);
 }
 
-int check_splitkv(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  int B, int H, int N, int d, float scale, int causal, int splits,
-                  const void* ws, size_t ws_bytes) {
-  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
-  if (rc != ATTN_OK) return rc;
+int check_splits(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 int B, int H, int Nq, int Nk, int d, int splits, const void* ws, size_t ws_bytes) {
   if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  if (BH * ((static_cast<int64_t>(N) + 127) / 128) * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (BH * ((static_cast<int64_t>(Nq) + 127) / 128) * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   if (splits == 1) return ATTN_OK;
-  const size_t need = splitkv_bytes(BH, N, d, splits, nullptr);
+  const size_t need = splitkv_bytes(BH, Nq, d, splits, nullptr);
   if (!ws || ws_bytes < need) return ATTN_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return ATTN_ERR_MISALIGNED;
-  const size_t tb = static_cast<size_t>(BH) * N * d * 2, lb = static_cast<size_t>(BH) * N * 4;
-  if (overlaps(ws, need, q, tb) || overlaps(ws, need, k, tb) || overlaps(ws, need, v, tb) ||
-      overlaps(ws, need, o, tb) || overlaps(ws, need, lse, lb))
+  const size_t qb = static_cast<size_t>(BH) * Nq * d * 2, kb = static_cast<size_t>(BH) * Nk * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * Nq * 4;
+  if (overlaps(ws, need, q, qb) || overlaps(ws, need, k, kb) || overlaps(ws, need, v, kb) ||
+      overlaps(ws, need, o, qb) || overlaps(ws, need, lse, lb))
     return ATTN_ERR_ALIAS;
   return ATTN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-             int d, float scale, int causal, void* stream) {
-  int rc = check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+// Every forward entry point lands here: checks, then the fused kernel and,
+// for split-KV, the merge kernel, all on `stream`.
+int fwd_general(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, float scale, int causal, int splits, void* ws,
+                size_t ws_bytes, void* stream) {
+  int rc = check_general(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal);
   if (rc != ATTN_OK) return rc;
+  if ((rc = check_splits(q, k, v, o, lse, B, H, Nq, Nk, d, splits, ws, ws_bytes)) != ATTN_OK)
+    return rc;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-  return launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, nullptr, ds,
-                    static_cast<cudaStream_t>(stream));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (splits == 1)
+    return launch_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 1, nullptr, nullptr, ds, st);
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  size_t lse_off = 0;
+  splitkv_bytes(BH, Nq, d, splits, &lse_off);
+  float* o_part = static_cast<float*>(ws);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + lse_off);
+  if ((rc = launch_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, splits, o_part, lse_part,
+                       ds, st)) != ATTN_OK)
+    return rc;
+  const cudaError_t e = ea51::launch_combine(d, o_part, lse_part, o, lse, BH * Nq, splits, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
 }
 
-size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
-  if (B < 1 || H < 1 || N < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
-  if (d != 64 && d != 128 && d != 256) return 0;
-  if (num_splits == 1) return 0;
-  return splitkv_bytes(static_cast<int64_t>(B) * H, N, d, num_splits, nullptr);
-}
-
-int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1) return 1;
+// Split count with the smallest modelled makespan (see include/attn_fwd.h).
+int split_model(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1)
+    return 1;
+  if (causal && Nk < Nq) return 1;
   const ea51::FwdVariant var = variant_for(d);
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t nq = (static_cast<int64_t>(N) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  const int64_t nq = (static_cast<int64_t>(Nq) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
   const int64_t ctas = BH * nq;
   if (ctas >= num_sms) return 1;  // a full wave already: splitting only adds the merge
   // Model: a CTA costs (key tiles it visits + 2) time units, CTAs start in
   // launch order (heaviest first) on the least-loaded multiprocessor, and a
   // split launch pays 5 % for the merge kernel and the workspace traffic.
-  // Pick the split count with the smallest modelled makespan.
   std::vector<int64_t> work;
   std::vector<int64_t> sm;
   double best = 0;
@@ -250,9 +270,10 @@ int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_
   for (int s = 1; s <= 16 && s <= kMaxSplits; ++s) {
     work.clear();
     for (int64_t qb = 0; qb < nq; ++qb) {
-      const int64_t last_row = std::min<int64_t>((qb + 1) * var.q_rows_per_cta, N) - 1;
-      const int64_t tiles = causal ? last_row / var.kv_rows + 1
-                                   : (static_cast<int64_t>(N) + var.kv_rows - 1) / var.kv_rows;
+      const int64_t last_key =
+          std::min<int64_t>((qb + 1) * var.q_rows_per_cta, Nq) - 1 + (Nk - Nq);
+      const int64_t tiles = causal ? last_key / var.kv_rows + 1
+                                   : (static_cast<int64_t>(Nk) + var.kv_rows - 1) / var.kv_rows;
       const int64_t share = (tiles + s - 1) / s;
       for (int i = 0; i < s; ++i) {
         const int64_t t = std::min<int64_t>(share, tiles - i * share);
@@ -278,28 +299,42 @@ int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_
   return best_s;
 }
 
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, void* stream) {
+  return fwd_general(q, k, v, o, lse, B, H, N, N, d, scale, causal, 1, nullptr, 0, stream);
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (d != 64 && d != 128 && d != 256) return 0;
+  if (num_splits == 1) return 0;
+  return splitkv_bytes(static_cast<int64_t>(B) * H, N, d, num_splits, nullptr);
+}
+
+int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
+  return split_model(B, H, N, N, d, causal, num_sms);
+}
+
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int N, int d, float scale, int causal, int num_splits, void* workspace,
                      size_t workspace_bytes, void* stream) {
-  int rc = check_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
-                         workspace_bytes);
-  if (rc != ATTN_OK) return rc;
-  DeviceState* ds = nullptr;
-  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (num_splits == 1)
-    return launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, nullptr, ds, st);
-  const int64_t BH = static_cast<int64_t>(B) * H;
-  size_t lse_off = 0;
-  splitkv_bytes(BH, N, d, num_splits, &lse_off);
-  float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
-  if ((rc = launch_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, o_part, lse_part, ds,
-                       st)) != ATTN_OK)
-    return rc;
-  const cudaError_t e = ea51::launch_combine(d, o_part, lse_part, o, lse, BH * N, num_splits, st);
-  if (e != cudaSuccess) return fail_cuda(e);
-  return ATTN_OK;
+  return fwd_general(q, k, v, o, lse, B, H, N, N, d, scale, causal, num_splits, workspace,
+                     workspace_bytes, stream);
+}
+
+int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_general(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, workspace,
+                     workspace_bytes, stream);
+}
+
+int attn_fwd_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
+  return split_model(B, H, Nq, Nk, d, causal, num_sms);
 }
 
 const char* attn_status_string(int status) {

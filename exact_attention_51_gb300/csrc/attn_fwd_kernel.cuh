@@ -208,17 +208,19 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
     qblk = cta % p.n_qblk;
   }
   t.row0 = qblk * L::NQ * BM;
-  const int nkv_all = (p.N + L::BN - 1) / L::BN;
+  const int nkv_all = (p.Nk + L::BN - 1) / L::BN;
   int nkv_abs[L::NQ];
   int nkv_cta = 0;
 #pragma unroll
   for (int q = 0; q < L::NQ; ++q) {
     const int r0 = t.row0 + q * BM;
-    if (r0 >= p.N) {
+    if (r0 >= p.Nq) {
       nkv_abs[q] = 0;
     } else if (CAUSAL) {
-      const int last_row = min(r0 + BM - 1, p.N - 1);
-      nkv_abs[q] = last_row / L::BN + 1;
+      // the last key visible to the tile's last query row (bottom-right
+      // aligned diagonal: query i sees keys j <= i + Nk - Nq)
+      const int last_key = min(r0 + BM - 1, p.Nq - 1) + p.causal_off;
+      nkv_abs[q] = last_key / L::BN + 1;
     } else {
       nkv_abs[q] = nkv_all;
     }
@@ -497,8 +499,8 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   float l = 0.f;
   if (n == 0) {
     // This split saw no key of this query tile: an empty partial.
-    if (SPLIT && grow < p.N)
-      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.N + static_cast<size_t>(t.bh) * p.N + grow] =
+    if (SPLIT && grow < p.Nq)
+      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + static_cast<size_t>(t.bh) * p.Nq + grow] =
           -INFINITY;
     return;
   }
@@ -517,11 +519,11 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     for (int ch = 0; ch < NCH; ++ch) tmem_ld_wait(s[ch]);
 
     const int key0 = (t.lo + j) * BN;
-    const bool masked = (CAUSAL && key0 + BN - 1 > r0) || (key0 + BN > p.N);
+    const bool masked = (CAUSAL && key0 + BN - 1 > r0 + p.causal_off) || (key0 + BN > p.Nk);
     int lim = BN;  // columns [0, lim) of this tile are visible to this row
     if (masked) {
-      lim = p.N - key0;
-      if (CAUSAL) lim = min(lim, grow - key0 + 1);
+      lim = p.Nk - key0;
+      if (CAUSAL) lim = min(lim, grow + p.causal_off - key0 + 1);
     }
 
     // row maximum of the raw scores (scale >= 0 keeps the arg-max)
@@ -580,14 +582,14 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with split-KV the
   // normalised fp32 partial O and the partial LSE go to the workspace.
   constexpr bool split_mode = SPLIT;
-  const bool valid = grow < p.N;
+  const bool valid = grow < p.Nq;
   ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
   if (!ok) return;
   tc_fence_after_sync();
   const float inv_l = 1.f / l;
-  const size_t row = static_cast<size_t>(t.bh) * p.N + (valid ? grow : 0);
+  const size_t row = static_cast<size_t>(t.bh) * p.Nq + (valid ? grow : 0);
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
-  float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.N + row) * D;
+  float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.Nq + row) * D;
 #pragma unroll
   for (int ch = 0; ch < D / 32; ++ch) {
     uint32_t ov[32];
@@ -617,7 +619,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   if (valid) {
     const float lse = (m_used + __log2f(l)) * kLn2;
     if constexpr (split_mode)
-      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.N + row] = lse;
+      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + row] = lse;
     else
       p.lse[row] = lse;
   }

@@ -7,16 +7,18 @@
 namespace ea51 {
 
 struct FwdParams {
-  void* o;               // bf16 [BH, N, D]
-  float* lse;            // fp32 [BH, N]
+  void* o;               // bf16 [BH, Nq, D]
+  float* lse;            // fp32 [BH, Nq]
   unsigned int* status;  // device-wide wait-timeout word (0 = clean)
-  int N;
+  int Nq;               // query rows per head
+  int Nk;               // key / value rows per head
+  int causal_off;       // Nk - Nq: query i sees keys j <= i + causal_off when causal
   int BH;
   int n_qblk;            // CTAs per head
   float scale_log2;      // scale * log2(e)
   // Split-KV: kv_splits CTAs share the key tiles of one query block; each
-  // writes its normalised partial O (fp32 [kv_splits][BH][N][D]) and its
-  // partial LSE (fp32 [kv_splits][BH][N], -inf when it saw no key) instead of
+  // writes its normalised partial O (fp32 [kv_splits][BH][Nq][D]) and its
+  // partial LSE (fp32 [kv_splits][BH][Nq], -inf when it saw no key) instead of
   // the final outputs.  kv_splits == 1 writes o / lse directly.
   int kv_splits;
   float* o_part;

@@ -140,6 +140,32 @@ ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int 
 ATTN_API int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms);
 
 /*
+ * Attention with a key length of its own (KV-cache shapes): q and o are
+ * [B,H,Nq,d], k and v [B,H,Nk,d], lse [B,H,Nq].  Causal puts the diagonal of
+ * the score matrix at its bottom-right corner -- query i sees keys
+ * j <= i + Nk - Nq, so the Nq queries act as the last Nq positions of a
+ * sequence whose keys are all Nk (the plainest reading of "the softmax of the
+ * triangular matrix", HN item 40939030, for a rectangular score matrix) --
+ * and needs Nk >= Nq.  Nq = Nk = N gives attn_fwd / attn_fwd_splitkv.
+ *
+ *   num_splits  1..64, as attn_fwd_splitkv; a decode-like call (small Nq,
+ *               long Nk) needs splits to occupy the GPU
+ *               (attn_fwd_kvcache_num_splits suggests a count).
+ *   workspace   as attn_fwd_splitkv, sized by
+ *               attn_fwd_splitkv_workspace_size(B, H, Nq, d, num_splits).
+ *   other arguments and errors as attn_fwd_splitkv; causal with Nk < Nq is
+ *   ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API int attn_fwd_kvcache(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* attn_fwd_splitkv_num_splits for attn_fwd_kvcache shapes.  Host-only. */
+ATTN_API int attn_fwd_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal,
+                                         int num_sms);
+
+/*
  * attn_fwd_splitkv without a caller-provided workspace.  The pages have no
  * counterpart of this entry point; it exists for callers that cannot
  * allocate device memory: a plugin whose host framework hands it only the

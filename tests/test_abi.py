@@ -177,3 +177,35 @@ def test_splitkv_rejects_bad_arguments(lib):
     q = list(p)
     q[0] = 0
     assert _splitkv(lib, q, 4, ws, need) == ea.ATTN_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ KV cache
+
+def _kvcache(lib, p, Nq, Nk, causal, splits=1, ws=None, ws_bytes=0, d=64):
+    return lib.attn_fwd_kvcache(*p, 1, 2, Nq, Nk, d, 0.125, causal, splits, ws, ws_bytes, None)
+
+
+def test_kvcache_rejects_bad_arguments(lib):
+    big = 1 << 24
+    p = ptrs(big)
+    # causal needs at least as many keys as queries
+    assert _kvcache(lib, p, 10, 9, 1) == ea.ATTN_ERR_INVALID_ARG
+    assert _kvcache(lib, p, 0, 9, 0) == ea.ATTN_ERR_INVALID_ARG
+    assert _kvcache(lib, p, 9, 0, 0) == ea.ATTN_ERR_INVALID_ARG
+    assert _kvcache(lib, p, 9, 9, 0, d=80) == ea.ATTN_ERR_INVALID_ARG
+    # o may not overlap the (longer) key tensor: keys span 1*2*4096*64*2 bytes
+    q, k, v, o, lse = p
+    assert _kvcache(lib, [q, k, v, k + 512 * 1024, lse], 16, 4096, 1) == ea.ATTN_ERR_ALIAS
+    # a split run needs its workspace
+    assert _kvcache(lib, p, 16, 4096, 1, splits=4) == ea.ATTN_ERR_INVALID_ARG
+
+
+def test_kvcache_split_heuristic(lib):
+    f = ea.attn_fwd_kvcache_num_splits
+    # decode: one query per head against a long cache -> split
+    assert f(1, 8, 1, 32768, 128, True, 152) >= 2
+    # Nq = Nk matches the square heuristic
+    for args in [(1, 4, 8192, 128, True), (1, 1, 8192, 128, False), (4, 16, 4096, 128, True)]:
+        B, H, N, d, c = args
+        assert f(B, H, N, N, d, c, 152) == ea.attn_fwd_splitkv_num_splits(B, H, N, d, c, 152)
+    assert f(1, 1, 9, 8, 128, True, 152) == 1  # invalid causal shape
