@@ -28,6 +28,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_ref.c")
+_SRC_BWD = os.path.join(_HERE, "attn_bwd_ref.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -37,18 +38,21 @@ _dbl = ctypes.c_double
 _vp = ctypes.c_void_p
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
-    """Compile ``src`` with gcc -O2 -fopenmp into ``out`` (shared object).
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH,
+          src_bwd: str | None = _SRC_BWD) -> str:
+    """Compile the forward source ``src`` (and the backward source
+    ``src_bwd`` unless None) with gcc -O2 -fopenmp into ``out``.
 
     Plain portable C: no -march flags, so the same source builds on x86_64 and
     aarch64 hosts.  Returns the path of the library.
     """
+    srcs = [src] + ([src_bwd] if src_bwd else [])
     if (not force and os.path.exists(out)
-            and os.path.getmtime(out) >= os.path.getmtime(src)):
+            and all(os.path.getmtime(out) >= os.path.getmtime(f) for f in srcs)):
         return out
     tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
-           "-o", tmp, src, "-lm"]
+           "-o", tmp, *srcs, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -73,6 +77,11 @@ def _bind(lib):
     lib.attn_ref_bf16_qk_rows.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _dbl,
                                           ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
     lib.attn_ref_bf16_qk_rows.restype = ctypes.c_int
+    if hasattr(lib, "attn_bwd_ref_f64"):
+        lib.attn_bwd_ref_f64.argtypes = [_vp] * 7 + [_i64] * 4 + [_dbl, ctypes.c_int, ctypes.c_int]
+        lib.attn_bwd_ref_f64.restype = ctypes.c_int
+        lib.attn_bwd_ref_bf16.argtypes = [_vp] * 7 + [_i64] * 4 + [_dbl, ctypes.c_int, ctypes.c_int]
+        lib.attn_bwd_ref_bf16.restype = ctypes.c_int
     lib.attn_ref_max_threads.argtypes = []
     lib.attn_ref_max_threads.restype = ctypes.c_int
     return lib
@@ -166,6 +175,38 @@ class Oracle:
             raise RuntimeError(f"oracle attn_ref_bf16_rows failed: {rc}")
         return o[:R], lse[:R]
 
+
+    # -- gradients (attn_bwd_ref.c): dQ, dK, dV for upstream gradient dO
+
+    def attn_bwd_f64(self, q, k, v, dout, causal: bool, scale: float, nthreads: int = 0):
+        """fp64 [B,H,N,d] inputs -> (dq, dk, dv) fp64 [B,H,N,d]."""
+        q, k, v, dout = (np.ascontiguousarray(a, dtype=np.float64) for a in (q, k, v, dout))
+        B, H, N, d = _shape4(q)
+        if k.shape != q.shape or v.shape != q.shape or dout.shape != q.shape:
+            raise ValueError("q, k, v, dout must share one [B,H,N,d] shape")
+        dq, dk, dv = (np.empty((B, H, N, d), np.float64) for _ in range(3))
+        rc = self.lib.attn_bwd_ref_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                       dout.ctypes.data, dq.ctypes.data, dk.ctypes.data,
+                                       dv.ctypes.data, B, H, N, d, float(scale),
+                                       int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_bwd_ref_f64 failed: {rc}")
+        return dq, dk, dv
+
+    def attn_bwd_bf16(self, q, k, v, dout, causal: bool, scale: float, nthreads: int = 0):
+        """torch bf16 CPU [B,H,N,d] inputs -> (dq, dk, dv) fp64."""
+        qb, kb, vb, gb = (_as_bf16_bits(t) for t in (q, k, v, dout))
+        B, H, N, d = _shape4(qb)
+        if kb.shape != qb.shape or vb.shape != qb.shape or gb.shape != qb.shape:
+            raise ValueError("q, k, v, dout must share one [B,H,N,d] shape")
+        dq, dk, dv = (np.empty((B, H, N, d), np.float64) for _ in range(3))
+        rc = self.lib.attn_bwd_ref_bf16(qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
+                                        gb.ctypes.data, dq.ctypes.data, dk.ctypes.data,
+                                        dv.ctypes.data, B, H, N, d, float(scale),
+                                        int(bool(causal)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_bwd_ref_bf16 failed: {rc}")
+        return dq, dk, dv
 
     # -- a key length of its own: q [B,H,Nq,d], k / v [B,H,Nk,d]; causal
     # -- means key j visible to query i iff j <= i + Nk - Nq (needs Nk >= Nq)

@@ -90,7 +90,8 @@ def test_pins_catch_mutant(desc, old, new):
     with tempfile.TemporaryDirectory() as td:
         msrc = os.path.join(td, "mutant.c")
         open(msrc, "w").write(src.replace(old, new))
-        lib = oracle.build(force=True, src=msrc, out=os.path.join(td, "libmutant.so"))
+        lib = oracle.build(force=True, src=msrc, out=os.path.join(td, "libmutant.so"),
+                           src_bwd=None)
         res = run_all(oracle.Oracle(oracle.load(lib)))
     failed = [k for k, v in res.items() if v]
     assert failed, f"no pin caught the planted mistake: {desc}"
