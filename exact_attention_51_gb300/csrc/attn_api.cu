@@ -185,6 +185,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   p.causal_off = Nk - Nq;
   p.BH = static_cast<int>(BH);
   p.n_qblk = (Nq + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  // Causal launch order interleaves the heaviest blocks of as many heads as
+  // keep their K and V within about half of L2 (64 MiB).
+  const double kv_head = 2.0 * Nk * d * 2;
+  const int64_t g = static_cast<int64_t>((64.0 * 1024 * 1024) / kv_head);
+  p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.kv_splits = kv_splits;
   p.o_part = o_part;

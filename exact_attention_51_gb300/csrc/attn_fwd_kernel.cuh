@@ -192,17 +192,17 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
   const int cta = blockIdx.x / splits;
   t.split = blockIdx.x - cta * splits;
   int qblk;
-  if (CAUSAL && L::NQ == 2) {
-    // Heaviest query blocks first across all heads (longest-processing-time
-    // order): the light blocks of every head fill the tail of the launch.
-    t.bh = cta % p.BH;
-    qblk = p.n_qblk - 1 - cta / p.BH;
-  } else if (CAUSAL) {
-    // One query tile per CTA re-reads K/V twice as often per FLOP; keeping a
-    // head's blocks together (heaviest first) keeps its K/V in L2, which
-    // measured faster than the global order here.
-    t.bh = cta / p.n_qblk;
-    qblk = p.n_qblk - 1 - cta % p.n_qblk;
+  if (CAUSAL) {
+    // Heaviest query blocks first (longest-processing-time order) across a
+    // group of heads_per_group heads: the light blocks fill the tail of the
+    // launch, and the group's K/V stays within L2 instead of every head's
+    // K/V streaming from HBM at once.
+    const int per_group = p.heads_per_group * p.n_qblk;
+    const int group = cta / per_group;
+    const int gs = min(p.heads_per_group, p.BH - group * p.heads_per_group);
+    const int within = cta - group * per_group;
+    t.bh = group * p.heads_per_group + within % gs;
+    qblk = p.n_qblk - 1 - within / gs;
   } else {
     t.bh = cta / p.n_qblk;
     qblk = cta % p.n_qblk;

@@ -15,6 +15,7 @@ struct FwdParams {
   int causal_off;       // Nk - Nq: query i sees keys j <= i + causal_off when causal
   int BH;
   int n_qblk;            // CTAs per head
+  int heads_per_group;   // causal launch order: heads whose query blocks interleave
   float scale_log2;      // scale * log2(e)
   // Split-KV: kv_splits CTAs share the key tiles of one query block; each
   // writes its normalised partial O (fp32 [kv_splits][BH][Nq][D]) and its
