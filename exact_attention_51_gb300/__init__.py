@@ -89,6 +89,10 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_kvcache.restype = _int
         lib.attn_fwd_kvcache_num_splits.argtypes = [_int, _int, _int, _int, _int, _int, _int]
         lib.attn_fwd_kvcache_num_splits.restype = _int
+        lib.attn_bwd.argtypes = [_vp] * 9 + [_int] * 4 + [_flt, _int, _vp, ctypes.c_size_t, _vp]
+        lib.attn_bwd.restype = _int
+        lib.attn_bwd_workspace_size.argtypes = [_int, _int, _int]
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.attn_selftest_wait_timeout.restype = _int
         _lib = lib
@@ -253,6 +257,46 @@ def attn_fwd_splitkv_noalloc(q, k, v, causal: bool = False, scale: float | None 
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv_noalloc")
     return out, lse
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, H, N))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of the forward pass: ``(dq, dk, dv)`` bf16 [B,H,N,d] for the
+    upstream gradient ``dout`` of ``o``, given the forward's ``o`` and ``lse``
+    (as returned by ``attn_fwd`` with the same ``causal`` and ``scale``).
+    Head dims 64 and 128.  The small fp32 workspace (2 * B*H*ceil128(N) floats)
+    is allocated with torch unless given."""
+    import torch
+    _check_qkv(q, k, v)
+    _check_qkv(o, dout, q)
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() \
+                or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    need = attn_bwd_workspace_size(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().attn_bwd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

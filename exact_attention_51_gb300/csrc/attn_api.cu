@@ -12,7 +12,9 @@
 #include <mutex>
 #include <vector>
 
+#include "attn_bwd.h"
 #include "attn_fwd.h"
+#include "bwd_dispatch.h"
 #include "fwd_dispatch.h"
 
 namespace {
@@ -374,6 +376,66 @@ int attn_fwd_device_status(void* stream, unsigned int* detail) {
 }
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+size_t attn_bwd_workspace_size(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+  return 2 * align256(static_cast<size_t>(B) * H * npad * 4);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  // the forward's checks cover q, k, v, o and lse (o and lse as outputs there:
+  // here they are inputs, so only their sizes / alignment matter)
+  int rc = check_general(q, k, v, o, lse, B, H, N, N, d, scale, causal);
+  if (rc != ATTN_OK && rc != ATTN_ERR_ALIAS) return rc;
+  if (d != 64 && d != 128) return ATTN_ERR_INVALID_ARG;
+  if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
+  if (!al(dout, 16) || !al(dq, 16) || !al(dk, 16) || !al(dv, 16) || !al(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_bwd_workspace_size(B, H, N);
+  if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const size_t tb = static_cast<size_t>(BH) * N * d * 2, lb = static_cast<size_t>(BH) * N * 4;
+  const void* ins[6] = {q, k, v, o, dout, lse};
+  const size_t in_bytes[6] = {tb, tb, tb, tb, tb, lb};
+  const void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {tb, tb, tb, need};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return ATTN_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return ATTN_ERR_ALIAS;
+  }
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  if ((rc = encode_map(&tq, q, BH, N, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, N, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, N, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tdo, dout, BH, N, d, 128)) != ATTN_OK) return rc;
+  ea51::BwdParams p{};
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  const int npad = (N + 127) / 128 * 128;
+  p.lse2 = static_cast<float*>(workspace);
+  p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    align256(static_cast<size_t>(BH) * npad * 4));
+  p.status = ds->status;
+  p.N = N;
+  p.Npad = npad;
+  p.BH = static_cast<int>(BH);
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const cudaError_t e = ea51::launch_bwd(&tq, &tk, &tv, &tdo, p, o, dout, lse, d, causal != 0,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
+}
+
 
 int attn_selftest_wait_timeout(unsigned int timeout_ms, void* stream) {
   if (timeout_ms < 1 || timeout_ms > 10000) return ATTN_ERR_INVALID_ARG;

@@ -1,0 +1,554 @@
+// Backward pass of the fused exact attention (gradients dQ, dK, dV) for
+// sm_103a.  For O = softmax(scale * Q K^T [+ causal mask]) V with upstream
+// gradient dO, and P recomputed from the forward's log-sum-exp:
+//
+//   P = exp(scale * Q K^T - LSE),  D_i = sum_c dO_ic O_ic
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q
+//
+// Three kernels, none of them writing an N x N matrix to HBM:
+//   preprocess  D and LSE * log2(e) per row into a padded workspace;
+//   dK/dV       one CTA per 128-key block: for every query block it
+//               recomputes S^T = K Q^T and dP^T = V dO^T in tensor memory,
+//               one thread per key row forms P^T and dS^T (bf16, written over
+//               the fp32 tiles), and the tensor core accumulates
+//               dV += P^T dO and dK += dS^T Q in tensor memory;
+//   dQ          one CTA per 128-query block: recomputes S and dP per key
+//               block, forms dS per query row, accumulates dQ += dS K.
+// S and dP are computed twice (once per kernel) so that no kernel needs a
+// transposed copy of dS or atomics: every MMA uses the operand layouts of the
+// forward kernel (K-major A/B from shared memory, or A from tensor memory
+// with an MN-major B).  The pages name the backward pass only as the part the
+// ~100-line kernel's author had not written ("Show HN: Flash Attention in
+// ~100 lines of CUDA"); the formulas are the derivative of the forward
+// definition.  Head dims 64 and 128 (the tensor memory holds S, dP and two
+// d-column accumulators).
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "attn_fwd_kernel.cuh"
+#include "bwd_dispatch.h"
+
+namespace ea51 {
+namespace {
+
+constexpr int BQ = 128;  // query rows per tile
+constexpr int BK = 128;  // key rows per tile
+
+template <int D>
+struct BwdLayout {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL = 128 * 128;  // one 64-column panel of a 128-row tile
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int STAGES = D == 64 ? 3 : 2;
+  // dK/dV kernel: K, V resident; ring of {Q, dO, lse', D} per query block
+  static constexpr int A_OFF_K = 0, A_OFF_V = TILE, A_OFF_RING = 2 * TILE;
+  static constexpr int A_STAGE = 2 * TILE + 2 * 512;
+  static constexpr int A_OFF_BAR = A_OFF_RING + STAGES * A_STAGE;
+  // dQ kernel: Q, dO resident; ring of {K, V} per key block
+  static constexpr int B_OFF_Q = 0, B_OFF_DO = TILE, B_OFF_RING = 2 * TILE;
+  static constexpr int B_STAGE = 2 * TILE;
+  static constexpr int B_OFF_BAR = B_OFF_RING + STAGES * B_STAGE;
+  // barriers (both kernels): 0 resident-full, [1, 1+ST) ring full,
+  // [1+ST, 1+2ST) ring empty, s_full, p_ready, final, drain
+  static constexpr int BAR_RES = 0, BAR_FULL = 1, BAR_EMPTY = 1 + STAGES, BAR_S = 1 + 2 * STAGES,
+                       BAR_P = BAR_S + 1, BAR_FINAL = BAR_P + 1, BAR_DRAIN = BAR_FINAL + 1,
+                       NBAR = BAR_DRAIN + 1;
+  static constexpr int A_SMEM = A_OFF_BAR + NBAR * 8 + 8 + 1024;
+  static constexpr int B_SMEM = B_OFF_BAR + NBAR * 8 + 8 + 1024;
+  // tensor memory: T1 = S^T or S, T2 = dP^T or dP, then the accumulators
+  static constexpr int T1 = 0, T2 = 128, ACC0 = 256, ACC1 = 256 + D;
+  static_assert(ACC1 + D <= 512 || D == 64, "tensor memory");
+  static_assert(A_SMEM <= 232448 && B_SMEM <= 232448, "shared memory");
+};
+
+struct BwdTile {
+  int bh, blk, n;  // head, this CTA's block, number of blocks it visits
+  int first;       // first visited block of the other operand
+};
+
+// 1-D bulk copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------------ preprocess
+
+__global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                      const __nv_bfloat16* __restrict__ dout,
+                                      const float* __restrict__ lse, float* __restrict__ lse2,
+                                      float* __restrict__ dsum, int N, int Npad, long long BH,
+                                      int d) {
+  // one warp per padded row
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= BH * Npad) return;
+  const long long bh = w / Npad;
+  const int i = static_cast<int>(w - bh * Npad);
+  float acc = 0.f;
+  float l2 = 0.f;
+  if (i < N) {
+    const long long row = bh * N + i;
+    for (int c = lane * 2; c < d; c += 64) {
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + row * d + c);
+      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + row * d + c);
+      acc += __bfloat162float(a.x) * __bfloat162float(g.x) + __bfloat162float(a.y) * __bfloat162float(g.y);
+    }
+    l2 = lse[row] * 1.4426950408889634f;
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    lse2[bh * Npad + i] = l2;
+    dsum[bh * Npad + i] = acc;
+  }
+}
+
+// ------------------------------------------------------------ dK / dV
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + L::A_OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::A_OFF_BAR + L::NBAR * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::A_OFF_BAR + L::NBAR * 8 + 4);
+  const Waiter w{abort_flag, p.status};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // tile: key block kb of head bh; causal visits query blocks kb..nblk-1
+  const int nblk = (p.N + 127) / 128;
+  const int bh = blockIdx.x / nblk;
+  const int kb = blockIdx.x % nblk;
+  const int q_first = CAUSAL ? kb : 0;
+  const int nq = nblk - q_first;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? 4u : 1u);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      const uint32_t rb = bar(L::BAR_RES);
+      mbar_arrive_expect_tx(rb, 2 * L::TILE);
+      for (int pn = 0; pn < L::PANELS; ++pn) {
+        tma_load_3d(sbase + L::A_OFF_K + pn * L::PANEL, &tm_k, rb, pn * 64, kb * 128, bh);
+        tma_load_3d(sbase + L::A_OFF_V + pn * L::PANEL, &tm_v, rb, pn * 64, kb * 128, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < nq; ++t) {
+        const int st = t % L::STAGES;
+        const uint32_t ph = static_cast<uint32_t>(t / L::STAGES) & 1u;
+        if (!wait_phase(bar(L::BAR_EMPTY + st), ph ^ 1u, w, kCodeProducerEmpty)) break;
+        const uint32_t fb = bar(L::BAR_FULL + st);
+        const uint32_t base = sbase + L::A_OFF_RING + st * L::A_STAGE;
+        const int qblk = q_first + t;
+        mbar_arrive_expect_tx(fb, 2 * L::TILE + 1024);
+        for (int pn = 0; pn < L::PANELS; ++pn) {
+          tma_load_3d(base + pn * L::PANEL, &tm_q, fb, pn * 64, qblk * 128, bh);
+          tma_load_3d(base + L::TILE + pn * L::PANEL, &tm_do, fb, pn * 64, qblk * 128, bh);
+        }
+        const size_t rowoff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(qblk) * 128;
+        bulk_load(base + 2 * L::TILE, p.lse2 + rowoff, 512, fb);
+        bulk_load(base + 2 * L::TILE + 512, p.dsum + rowoff, 512, fb);
+        ++issued;
+      }
+      if (*w.abort_flag) {
+        drain_phase(bar(L::BAR_RES), 0u, w, kCodeDrain);
+        for (int t = max(0, issued - L::STAGES); t < issued; ++t)
+          drain_phase(bar(L::BAR_FULL + t % L::STAGES), static_cast<uint32_t>(t / L::STAGES) & 1u,
+                      w, kCodeDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA
+    const uint32_t leader = elect_one();
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);  // S^T, dP^T: both K-major
+    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);     // dV, dK: B MN-major
+    bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
+    const uint64_t dK0 = sdesc_sw128(sbase + L::A_OFF_K, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sbase + L::A_OFF_V, 16, 1024);
+    for (int t = 0; t < nq && ok; ++t) {
+      const int st = t % L::STAGES;
+      ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
+                           kCodeMmaKV);
+      if (!ok) break;
+      const uint32_t base = sbase + L::A_OFF_RING + st * L::A_STAGE;
+      const uint64_t qK = sdesc_sw128(base, 16, 1024);                 // Q as K-major B
+      const uint64_t oK = sdesc_sw128(base + L::TILE, 16, 1024);       // dO as K-major B
+      const uint64_t qM = sdesc_sw128(base, L::PANEL, 1024);           // Q as MN-major B
+      const uint64_t oM = sdesc_sw128(base + L::TILE, L::PANEL, 1024); // dO as MN-major B
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T1, dK0 + off, qK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // S^T
+      }
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T2, dV0 + off, oK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // dP^T
+      }
+      mma_commit(bar(L::BAR_S), leader);
+      ok = warp_wait_phase(bar(L::BAR_P), static_cast<uint32_t>(t) & 1u, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < BQ / 16; ++k) {
+        const uint32_t bo = (k * 16 * 128) >> 4;
+        const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+        mma_ts(tmem + L::ACC0, tmem + L::T1 + k * 8, oM + bo, kIdescTS, acc, leader);  // dV
+        mma_ts(tmem + L::ACC1, tmem + L::T2 + k * 8, qM + bo, kIdescTS, acc, leader);  // dK
+      }
+      mma_commit(bar(L::BAR_EMPTY + st), leader);
+    }
+    if (ok) mma_commit(bar(L::BAR_FINAL), leader);
+    if (!ok) {
+      mma_commit(bar(L::BAR_DRAIN), leader);
+      drain_phase(bar(L::BAR_DRAIN), 0u, w, kCodeDrain);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------- P^T, dS^T: one thread per key
+    const int r = warp * 32 + lane;  // key row in the block == TMEM lane
+    const int key = kb * 128 + r;
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < nq && ok; ++t) {
+      const int st = t % L::STAGES;
+      const int qblk = q_first + t;
+      // the stage's LSE / D rows were written by the TMA: wait on its barrier
+      // too before reading them from shared memory
+      ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
+                           kCodeSoftS);
+      if (ok) ok = warp_wait_phase(bar(L::BAR_S), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::A_OFF_RING + st * L::A_STAGE + 2 * L::TILE);
+      const float* dsm = lse2 + 128;
+      const bool diag = CAUSAL && qblk == kb;     // key > query masked inside
+      const bool tail = qblk * 128 + 128 > p.N;  // queries >= N masked
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(tmem + lb + L::T1 + ch * 32, s);
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + ch * 32, dp);
+        tmem_ld_wait(s);
+        tmem_ld_wait(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = ch * 32 + 2 * e + h;  // query within the block
+            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), c, -lse2[col]));
+            if ((diag && key > qblk * 128 + col) || (tail && qblk * 128 + col >= p.N)) pp = 0.f;
+            pv[h] = pp;
+            dv[h] = pp * (__uint_as_float(dp[2 * e + h]) - dsm[col]);
+          }
+          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          dk[e] = pack_bf16x2(dv[0], dv[1]);
+        }
+        // chunk ch's bf16 pairs land on columns 16ch..16ch+15, which belong
+        // to chunks already read (ch/2), never to one still to be read
+        tmem_st_32x32b_x16(tmem + lb + L::T1 + ch * 16, pk);
+        tmem_st_32x32b_x16(tmem + lb + L::T2 + ch * 16, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::BAR_P));
+    }
+    if (ok && nq > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
+    if (ok) {
+      tc_fence_after_sync();
+      const bool valid = key < p.N;
+      const size_t row = static_cast<size_t>(bh) * p.N + (valid ? key : 0);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst_row = (which == 0 ? p.dv : p.dk) + row * D;
+        const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t a[32];
+          tmem_ld_32x32b_x32(tmem + lb + (which == 0 ? L::ACC0 : L::ACC1) + ch * 32, a);
+          tmem_ld_wait(a);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + ch * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ dQ
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar0 = sbase + L::B_OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::B_OFF_BAR + L::NBAR * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::B_OFF_BAR + L::NBAR * 8 + 4);
+  const Waiter w{abort_flag, p.status};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // tile: query block qb of head bh (heaviest first when causal); visits key
+  // blocks 0..qb (causal) or all
+  const int nblk = (p.N + 127) / 128;
+  const int bh = blockIdx.x % p.BH;
+  const int qb = CAUSAL ? nblk - 1 - static_cast<int>(blockIdx.x / p.BH) : static_cast<int>(blockIdx.x / p.BH);
+  const int nk = CAUSAL ? qb + 1 : nblk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? 4u : 1u);
+    *abort_flag = 0u;
+    fence_mbarrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint32_t rb = bar(L::BAR_RES);
+      mbar_arrive_expect_tx(rb, 2 * L::TILE);
+      for (int pn = 0; pn < L::PANELS; ++pn) {
+        tma_load_3d(sbase + L::B_OFF_Q + pn * L::PANEL, &tm_q, rb, pn * 64, qb * 128, bh);
+        tma_load_3d(sbase + L::B_OFF_DO + pn * L::PANEL, &tm_do, rb, pn * 64, qb * 128, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < nk; ++t) {
+        const int st = t % L::STAGES;
+        const uint32_t ph = static_cast<uint32_t>(t / L::STAGES) & 1u;
+        if (!wait_phase(bar(L::BAR_EMPTY + st), ph ^ 1u, w, kCodeProducerEmpty)) break;
+        const uint32_t fb = bar(L::BAR_FULL + st);
+        const uint32_t base = sbase + L::B_OFF_RING + st * L::B_STAGE;
+        mbar_arrive_expect_tx(fb, 2 * L::TILE);
+        for (int pn = 0; pn < L::PANELS; ++pn) {
+          tma_load_3d(base + pn * L::PANEL, &tm_k, fb, pn * 64, t * 128, bh);
+          tma_load_3d(base + L::TILE + pn * L::PANEL, &tm_v, fb, pn * 64, t * 128, bh);
+        }
+        ++issued;
+      }
+      if (*w.abort_flag) {
+        drain_phase(bar(L::BAR_RES), 0u, w, kCodeDrain);
+        for (int t = max(0, issued - L::STAGES); t < issued; ++t)
+          drain_phase(bar(L::BAR_FULL + t % L::STAGES), static_cast<uint32_t>(t / L::STAGES) & 1u,
+                      w, kCodeDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    const uint32_t leader = elect_one();
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);
+    bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
+    const uint64_t qA = sdesc_sw128(sbase + L::B_OFF_Q, 16, 1024);
+    const uint64_t oA = sdesc_sw128(sbase + L::B_OFF_DO, 16, 1024);
+    for (int t = 0; t < nk && ok; ++t) {
+      const int st = t % L::STAGES;
+      ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
+                           kCodeMmaKV);
+      if (!ok) break;
+      const uint32_t base = sbase + L::B_OFF_RING + st * L::B_STAGE;
+      const uint64_t kK = sdesc_sw128(base, 16, 1024);
+      const uint64_t vK = sdesc_sw128(base + L::TILE, 16, 1024);
+      const uint64_t kM = sdesc_sw128(base, L::PANEL, 1024);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T1, qA + off, kK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // S
+      }
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T2, oA + off, vK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // dP
+      }
+      mma_commit(bar(L::BAR_S), leader);
+      ok = warp_wait_phase(bar(L::BAR_P), static_cast<uint32_t>(t) & 1u, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k) {
+        const uint32_t bo = (k * 16 * 128) >> 4;
+        mma_ts(tmem + L::ACC0, tmem + L::T1 + k * 8, kM + bo, kIdescTS, (t > 0 || k > 0) ? 1u : 0u,
+               leader);  // dQ += dS K
+      }
+      mma_commit(bar(L::BAR_EMPTY + st), leader);
+    }
+    if (ok) mma_commit(bar(L::BAR_FINAL), leader);
+    if (!ok) {
+      mma_commit(bar(L::BAR_DRAIN), leader);
+      drain_phase(bar(L::BAR_DRAIN), 0u, w, kCodeDrain);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    const int r = warp * 32 + lane;  // query row in the block == TMEM lane
+    const int qrow = qb * 128 + r;
+    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.scale_log2;
+    const size_t prow = static_cast<size_t>(bh) * p.Npad + qrow;
+    const float l2 = p.lse2[prow];
+    const float dsum = p.dsum[prow];
+    bool ok = true;
+    for (int t = 0; t < nk && ok; ++t) {
+      ok = warp_wait_phase(bar(L::BAR_S), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const bool diag = CAUSAL && t == qb;
+      const bool tail = t * 128 + 128 > p.N;
+      int lim = 128;  // keys [0, lim) of this block are visible
+      if (tail) lim = p.N - t * 128;
+      if (diag) lim = min(lim, qrow - t * 128 + 1);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(tmem + lb + L::T1 + ch * 32, s);
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + ch * 32, dp);
+        tmem_ld_wait(s);
+        tmem_ld_wait(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float dv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = ch * 32 + 2 * e + h;
+            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), c, -l2));
+            if ((diag || tail) && col >= lim) pp = 0.f;
+            dv[h] = pp * (__uint_as_float(dp[2 * e + h]) - dsum);
+          }
+          dk[e] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st_32x32b_x16(tmem + lb + L::T1 + ch * 16, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::BAR_P));
+    }
+    if (ok && nk > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
+    if (ok) {
+      tc_fence_after_sync();
+      const bool valid = qrow < p.N;
+      __nv_bfloat16* dst_row = p.dq + (static_cast<size_t>(bh) * p.N + (valid ? qrow : 0)) * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tmem + lb + L::ACC0 + ch * 32, a);
+        tmem_ld_wait(a);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * p.scale, __uint_as_float(a[2 * e + 1]) * p.scale);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + ch * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                         const CUtensorMap* tdo, const BwdParams& p, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  cudaError_t e;
+  if ((e = set_smem(bwd_dkdv_kernel<D, CAUSAL>, L::A_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_dq_kernel<D, CAUSAL>, L::B_SMEM)) != cudaSuccess) return e;
+  const unsigned nblk = static_cast<unsigned>((p.N + 127) / 128);
+  const unsigned grid = nblk * static_cast<unsigned>(p.BH);
+  bwd_dkdv_kernel<D, CAUSAL><<<grid, 256, L::A_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_dq_kernel<D, CAUSAL><<<grid, 256, L::B_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                       const CUtensorMap* tdo, const BwdParams& p, const void* o, const void* dout,
+                       const float* lse, int d, bool causal, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.BH) * p.Npad;
+  const long long threads = rows * 32;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  bwd_preprocess_kernel<<<blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, p.lse2,
+      p.dsum, p.N, p.Npad, p.BH, d);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (d == 64) return causal ? launch_bwd_d<64, true>(tq, tk, tv, tdo, p, stream)
+                             : launch_bwd_d<64, false>(tq, tk, tv, tdo, p, stream);
+  if (d == 128) return causal ? launch_bwd_d<128, true>(tq, tk, tv, tdo, p, stream)
+                              : launch_bwd_d<128, false>(tq, tk, tv, tdo, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ea51
