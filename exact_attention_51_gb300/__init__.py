@@ -93,6 +93,11 @@ def load_library(path: str = LIB_PATH):
         lib.attn_bwd.restype = _int
         lib.attn_bwd_workspace_size.argtypes = [_int, _int, _int]
         lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_fp8.argtypes = [_vp, _vp, _vp, _flt, _flt, _flt, _vp, _vp, _int, _int, _int,
+                                     _int, _flt, _int, _vp, ctypes.c_size_t, _vp]
+        lib.attn_fwd_fp8.restype = _int
+        lib.attn_fwd_fp8_workspace_size.argtypes = [_int, _int, _int, _int]
+        lib.attn_fwd_fp8_workspace_size.restype = ctypes.c_size_t
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.attn_selftest_wait_timeout.restype = _int
         _lib = lib
@@ -157,6 +162,56 @@ def _outputs(q, out, lse):
     elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
             or lse.device != q.device:
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
+    return out, lse
+
+
+def attn_fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_fwd_fp8_workspace_size(B, H, N, d))
+
+
+def attn_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
+                 causal: bool = False, scale: float | None = None, out=None, lse=None,
+                 workspace=None, stream=None):
+    """Attention forward on e4m3 inputs: q, k, v CUDA tensors [B, H, N, 128]
+    of dtype float8_e4m3fn (or uint8 holding e4m3 codes), element x meaning
+    ``descale * x``.  Returns ``(o, lse)``: o bf16 [B,H,N,d], lse fp32
+    [B,H,N].  The V-transpose workspace is allocated with torch unless
+    given."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda \
+                or t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be a CUDA float8_e4m3fn (or uint8) tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, H, N, d]")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    elif out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
+    need = attn_fwd_fp8_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = load_library().attn_fwd_fp8(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
+            float(descale_v), out.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
+            int(bool(causal)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return out, lse
 
 

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "attn_bwd.h"
+#include "attn_fp8.h"
 #include "attn_fwd.h"
 #include "bwd_dispatch.h"
 #include "fwd_dispatch.h"
@@ -120,25 +121,32 @@ int device_state(DeviceState** out) {
   return ATTN_OK;
 }
 
-// [BH, N, d] bf16 viewed as a 3-D tensor (d innermost); box = 64 columns
-// (one 128-byte swizzle span) x `rows` rows x one head.  Rows past N read as
-// zeros, so a ragged last tile never touches the next head.
-int encode_map(CUtensorMap* map, const void* base, int64_t BH, int N, int d, int rows) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+// A [BH, rows, cols] tensor (cols innermost, `pitch` elements between rows)
+// with a box of 128 bytes of columns x `box_rows` rows x one head, 128-byte
+// swizzle.  Rows and columns past the extents read as zeros, so a ragged last
+// tile never touches the next head.
+int encode_tiled(CUtensorMap* map, const void* base, CUtensorMapDataType type, int elem_bytes,
+                 int64_t BH, int64_t rows, int64_t cols, int64_t pitch, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(N)};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch * elem_bytes),
+                                 static_cast<cuuint64_t>(pitch * elem_bytes * rows)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes),
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estride[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-                              dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estride,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_cuda_error = static_cast<int>(r);
     return ATTN_ERR_LAUNCH;
   }
   return ATTN_OK;
+}
+
+// [BH, N, d] bf16: box = 64 columns (one 128-byte swizzle span) x `rows` rows.
+int encode_map(CUtensorMap* map, const void* base, int64_t BH, int N, int d, int rows) {
+  return encode_tiled(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, BH, N, d, d, rows);
 }
 
 }  // namespace
@@ -376,6 +384,73 @@ int attn_fwd_device_status(void* stream, unsigned int* detail) {
 }
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d != 128) return 0;
+  const size_t n_pad = (static_cast<size_t>(N) + 15) / 16 * 16;
+  return align256(static_cast<size_t>(B) * H * d * n_pad);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
+                 float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
+                 int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || d != 128) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  for (const float ds : {descale_q, descale_k, descale_v})
+    if (!std::isfinite(ds) || ds <= 0.f) return ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > 0x7fffffffLL || BH * ((static_cast<int64_t>(N) + 127) / 128) > 0x7fffffffLL ||
+      N > 0x7fffffff - 16)
+    return ATTN_ERR_INVALID_ARG;
+  const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
+  if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4) || !al(workspace, 256))
+    return ATTN_ERR_MISALIGNED;
+  const size_t need = attn_fwd_fp8_workspace_size(B, H, N, d);
+  if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t in_bytes = static_cast<size_t>(BH) * N * d;  // one byte per e4m3 element
+  const void* outs[3] = {o, lse, workspace};
+  const size_t out_bytes[3] = {in_bytes * 2, static_cast<size_t>(BH) * N * 4, need};
+  for (int i = 0; i < 3; ++i) {
+    for (const void* in : {q, k, v})
+      if (overlaps(outs[i], out_bytes[i], in, in_bytes)) return ATTN_ERR_ALIAS;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return ATTN_ERR_ALIAS;
+  }
+  DeviceState* ds = nullptr;
+  int rc;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n_pad = (N + 15) / 16 * 16;
+  cudaError_t e = ea51::launch_transpose_v8(v, workspace, BH, N, d, n_pad, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  const ea51::FwdVariant var = ea51::fwd_variant_e4m3_d128();
+  alignas(64) CUtensorMap tq, tk, tv;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if ((rc = encode_tiled(&tq, q, u8, 1, BH, N, d, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_tiled(&tk, k, u8, 1, BH, N, d, d, var.kv_rows)) != ATTN_OK) return rc;
+  // V^T [BH, d, n_pad]: rows are the d columns of V, keys innermost
+  if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, N, n_pad, d)) != ATTN_OK) return rc;
+  ea51::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.status = ds->status;
+  p.Nq = N;
+  p.Nk = N;
+  p.causal_off = 0;
+  p.BH = static_cast<int>(BH);
+  p.n_qblk = (N + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  const double kv_head = 2.0 * N * d;
+  const int64_t g = static_cast<int64_t>((64.0 * 1024 * 1024) / kv_head);
+  p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * descale_q * descale_k *
+                                    1.4426950408889634);
+  p.o_scale = descale_v;
+  p.kv_splits = 1;
+  e = var.launch(&tq, &tk, &tv, p, causal != 0, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  return ATTN_OK;
+}
 
 size_t attn_bwd_workspace_size(int B, int H, int N) {
   if (B < 1 || H < 1 || N < 1) return 0;

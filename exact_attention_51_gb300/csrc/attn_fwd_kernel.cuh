@@ -60,16 +60,23 @@ struct Shape<256> {
   static constexpr int BN = 64, NQ = 1, NSB = 2, STAGES = 4;
 };
 
-template <int D>
+// F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots);
+// the V tile is then stored transposed (D rows of BN keys) so that both MMAs
+// read K-major operands.
+template <int D, bool F8 = false>
 struct Layout {
+  static constexpr int EB = F8 ? 1 : 2;  // bytes per Q/K/V element
   static constexpr int BN = Shape<D>::BN, NQ = Shape<D>::NQ, NSB = Shape<D>::NSB,
-                       STAGES = Shape<D>::STAGES;
-  static constexpr int PANELS = D / 64;  // 128-byte (64 x bf16) column panels per row
+                       STAGES = F8 ? 2 * Shape<D>::STAGES : Shape<D>::STAGES;
+  static constexpr int PANELS = D * EB / 128;  // 128-byte column panels per Q/K row
+  static constexpr int PANEL_ELEMS = 128 / EB;
+  static constexpr int KSTEPS_QK = D * EB / 32;   // 32-byte K-steps of S = Q K^T
+  static constexpr int KSTEPS_PV = BN * EB / 32;  // and of O += P V
   static constexpr bool SPLIT_P = BN >= 128;  // hand P to the MMA warp in two halves
   static constexpr int Q_PANEL = BM * 128;
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * EB;
   static constexpr int KV_PANEL = BN * 128;
-  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int KV_BYTES = BN * D * EB;
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = NQ * Q_BYTES;
@@ -108,6 +115,7 @@ struct Layout {
                 "register split exceeds the launch budget");
 
   static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
+  static_assert(!F8 || (D == 128 && BN == 128), "e4m3 tiles: d = 128, 128 keys (one 128-byte row)");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1024-byte tile alignment");
@@ -235,11 +243,11 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
   return t;
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                               Waiter w) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   int nkv = 0;
@@ -251,8 +259,8 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
       mbar_arrive_expect_tx(fb, L::Q_BYTES);
 #pragma unroll
       for (int pn = 0; pn < L::PANELS; ++pn)
-        tma_load_3d(sbase + L::OFF_Q + q * L::Q_BYTES + pn * L::Q_PANEL, tm_q, fb, pn * 64,
-                    t.row0 + q * BM, t.bh);
+        tma_load_3d(sbase + L::OFF_Q + q * L::Q_BYTES + pn * L::Q_PANEL, tm_q, fb,
+                    pn * L::PANEL_ELEMS, t.row0 + q * BM, t.bh);
     }
   }
   const int total = 2 * nkv;  // K_0, V_0, K_1, V_1, ...
@@ -265,10 +273,15 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     mbar_arrive_expect_tx(fb, L::KV_BYTES);
     const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
     const int key0 = (t.lo + (i >> 1)) * L::BN;
+    if (F8 && (i & 1)) {
+      // transposed V: one box of D rows x BN keys (keys innermost)
+      tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES, map, fb, key0, 0, t.bh);
+    } else {
 #pragma unroll
-    for (int pn = 0; pn < L::PANELS; ++pn)
-      tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb, pn * 64, key0,
-                  t.bh);
+      for (int pn = 0; pn < L::PANELS; ++pn)
+        tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb,
+                    pn * L::PANEL_ELEMS, key0, t.bh);
+    }
     ++issued;
   }
   if (*w.abort_flag) {
@@ -285,12 +298,22 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 // Runs on a whole warp with warp-uniform control flow (so the descriptors
 // stay in uniform registers); one elected lane issues every tcgen05.mma and
 // tcgen05.commit.
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t, Waiter w) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
   constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
-  constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, false);  // A=Q, B=K: both K-major
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, true);    // A=P (tmem), B=V MN-major
+  // A=Q, B=K: both K-major.  A=P (tmem), B=V: MN-major in bf16, K-major for
+  // the transposed e4m3 V tile.
+  constexpr uint32_t kIdescQK = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
+  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, true);
+  auto mma_s = [](uint32_t d_t, uint64_t a, uint64_t b, uint32_t acc, uint32_t issue) {
+    if constexpr (F8) mma_ss_f8(d_t, a, b, kIdescQK, acc, issue);
+    else mma_ss(d_t, a, b, kIdescQK, acc, issue);
+  };
+  auto mma_pv = [](uint32_t d_t, uint32_t a_t, uint64_t b, uint32_t acc, uint32_t issue) {
+    if constexpr (F8) mma_ts_f8(d_t, a_t, b, kIdescPV, acc, issue);
+    else mma_ts(d_t, a_t, b, kIdescPV, acc, issue);
+  };
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t leader = elect_one();
@@ -319,17 +342,21 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
     const uint64_t b0 = sdesc_sw128(slot_addr(ks), 16, 1024);
     const uint32_t d_t = tmem + L::s_col(q, b);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
+    for (int k = 0; k < L::KSTEPS_QK; ++k) {
       const uint32_t ao = ((k / 4) * L::Q_PANEL + (k % 4) * 32) >> 4;
       const uint32_t bo = ((k / 4) * L::KV_PANEL + (k % 4) * 32) >> 4;
-      mma_ss(d_t, a0 + ao, b0 + bo, kIdescQK, k > 0 ? 1u : 0u, leader);
+      mma_s(d_t, a0 + ao, b0 + bo, k > 0 ? 1u : 0u, leader);
     }
     mma_commit(bar(L::B_SFULL + q * NSB + b), leader);
   };
   // O_q (+)= P(q, b) V with V in ring slot `vs`; waits for each half of P
   // (keys [0, BN/2) then [BN/2, BN)) before issuing its K-steps.
   auto issue_pv = [&](int q, int b, int vs, bool accumulate, uint32_t pph) {
-    const uint64_t b0 = sdesc_sw128(slot_addr(vs), L::KV_PANEL, 1024);
+    // bf16 V: MN-major, a 16-key K-step spans 16 rows of 128 bytes; e4m3 V^T:
+    // K-major, a 32-key K-step is 32 bytes along each 128-byte row.  Either
+    // way a K-step of P is 8 tensor-memory columns (2 bf16 or 4 e4m3 each).
+    const uint64_t b0 = F8 ? sdesc_sw128(slot_addr(vs), 16, 1024)
+                           : sdesc_sw128(slot_addr(vs), L::KV_PANEL, 1024);
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
 #pragma unroll
@@ -340,9 +367,9 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
         return false;
       tc_fence_after_sync();
 #pragma unroll
-      for (int k = h * (BN / 16 / NH); k < (h + 1) * (BN / 16 / NH); ++k) {
-        const uint32_t bo = (k * 16 * 128) >> 4;
-        mma_ts(d_t, a_t + k * 8, b0 + bo, kIdescPV, (accumulate || k > 0) ? 1u : 0u, leader);
+      for (int k = h * (L::KSTEPS_PV / NH); k < (h + 1) * (L::KSTEPS_PV / NH); ++k) {
+        const uint32_t bo = F8 ? (k * 32) >> 4 : (k * 16 * 128) >> 4;
+        mma_pv(d_t, a_t + k * 8, b0 + bo, (accumulate || k > 0) ? 1u : 0u, leader);
       }
     }
     mma_commit(bar(L::B_ODONE + q), leader);
@@ -476,10 +503,53 @@ __device__ __forceinline__ float exp_store(const uint32_t (&s)[NCH][32], int lim
   return f2_sum(f2_add(acc[0], acc[1]));
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+// e4m3 form of exp_store: 2^kF8Shift * exp2(s * c - m) as e4m3, four per
+// tensor-memory column at [CH0 * 8, CH1 * 8); returns the sum of the fp32
+// (shifted) values.
+template <int NCH, int CH0, int CH1, bool MASKED>
+__device__ __forceinline__ float exp_store_f8(const uint32_t (&s)[NCH][32], int lim, float c,
+                                              float m, uint32_t s_t) {
+  const f32x2 cc = f2_pack(c, c), nm = f2_pack(-m, -m);
+  f32x2 acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+  for (int ch = CH0; ch < CH1; ++ch) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float p4[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = 4 * e + 2 * h;
+        const f32x2 x =
+            f2_fma(f2_pack(__uint_as_float(s[ch][i]), __uint_as_float(s[ch][i + 1])), cc, nm);
+        float t0, t1;
+        f2_unpack(x, t0, t1);
+        float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+        if (MASKED) {
+          p0 = (ch * 32 + i < lim) ? p0 : 0.f;
+          p1 = (ch * 32 + i + 1 < lim) ? p1 : 0.f;
+        }
+        p4[2 * h] = p0;
+        p4[2 * h + 1] = p1;
+        acc[h] = f2_add(acc[h], f2_pack(p0, p1));
+      }
+      pk[e] = pack_e4m3x4(p4[0], p4[1], p4[2], p4[3]);
+    }
+    tmem_st_32x32b_x8(s_t + ch * 8, pk);
+  }
+  return f2_sum(f2_add(acc[0], acc[1]));
+}
+
+// e4m3 P is stored scaled by 2^kF8Shift: with the rescale threshold of 2^1
+// its values stay at or below 2^8 (e4m3 saturates at 448) and weights down to
+// 2^-13 of the row maximum stay normal numbers (3 mantissa bits).
+constexpr float kF8Shift = 7.0f;
+static_assert(kF8Shift + kRescaleThreshold <= 8.0f, "e4m3 P must stay below 448");
+
+template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                              const FwdParams& p, Waiter w) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
   constexpr int BN = L::BN, NSB = L::NSB;
   constexpr int NCH = BN / 32;  // 32-column chunks of an S row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -562,15 +632,27 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     // P.V starts before the second half is computed; 64-key tiles send it
     // whole (the second barrier round trip costs more than it overlaps).
     constexpr int H = L::SPLIT_P ? NCH / 2 : NCH;
-    l += masked ? exp_store<NCH, 0, H, true>(s, lim, c, m_used, s_t)
-                : exp_store<NCH, 0, H, false>(s, lim, c, m_used, s_t);
+    if constexpr (F8) {
+      const float m_f8 = m_used - kF8Shift;
+      l += masked ? exp_store_f8<NCH, 0, H, true>(s, lim, c, m_f8, s_t)
+                  : exp_store_f8<NCH, 0, H, false>(s, lim, c, m_f8, s_t);
+    } else {
+      l += masked ? exp_store<NCH, 0, H, true>(s, lim, c, m_used, s_t)
+                  : exp_store<NCH, 0, H, false>(s, lim, c, m_used, s_t);
+    }
     if constexpr (L::SPLIT_P) {
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2));
-      l += masked ? exp_store<NCH, H, NCH, true>(s, lim, c, m_used, s_t)
-                  : exp_store<NCH, H, NCH, false>(s, lim, c, m_used, s_t);
+      if constexpr (F8) {
+        const float m_f8 = m_used - kF8Shift;
+        l += masked ? exp_store_f8<NCH, H, NCH, true>(s, lim, c, m_f8, s_t)
+                    : exp_store_f8<NCH, H, NCH, false>(s, lim, c, m_f8, s_t);
+      } else {
+        l += masked ? exp_store<NCH, H, NCH, true>(s, lim, c, m_used, s_t)
+                    : exp_store<NCH, H, NCH, false>(s, lim, c, m_used, s_t);
+      }
     }
     tmem_st_wait();
     tc_fence_before_sync();
@@ -586,7 +668,9 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
   if (!ok) return;
   tc_fence_after_sync();
-  const float inv_l = 1.f / l;
+  // e4m3: O and l both carry the 2^kF8Shift factor; V's dequantisation
+  // scale multiplies O.
+  const float inv_l = F8 ? p.o_scale / l : 1.f / l;
   const size_t row = static_cast<size_t>(t.bh) * p.Nq + (valid ? grow : 0);
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
   float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.Nq + row) * D;
@@ -617,7 +701,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     }
   }
   if (valid) {
-    const float lse = (m_used + __log2f(l)) * kLn2;
+    const float lse = (m_used + __log2f(l) - (F8 ? kF8Shift : 0.f)) * kLn2;
     if constexpr (split_mode)
       p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + row] = lse;
     else
@@ -625,11 +709,11 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   }
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
-__global__ void __launch_bounds__(Layout<D>::THREADS, 1)
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false>
+__global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -668,16 +752,16 @@ __global__ void __launch_bounds__(Layout<D>::THREADS, 1)
   // split differs per path), then meets the others at the teardown barrier.
   if (warp < 4 * L::NQ) {
     if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
-    softmax_role<D, CAUSAL, SPLIT>(warp >> 2, tmem, sbase, t, p, w);
+    softmax_role<D, CAUSAL, SPLIT, F8>(warp >> 2, tmem, sbase, t, p, w);
     tc_fence_before_sync();
     __syncthreads();
   } else {
     if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
     if (warp == L::TMA_WARP) {
-      if (lane == 0) producer_role<D, CAUSAL, SPLIT>(&tm_q, &tm_k, &tm_v, sbase, t, w);
+      if (lane == 0) producer_role<D, CAUSAL, SPLIT, F8>(&tm_q, &tm_k, &tm_v, sbase, t, w);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
-      mma_role<D, CAUSAL, SPLIT>(tmem, sbase, t, w);
+      mma_role<D, CAUSAL, SPLIT, F8>(tmem, sbase, t, w);
       __syncwarp();
     }
     tc_fence_before_sync();

@@ -16,7 +16,8 @@ struct FwdParams {
   int BH;
   int n_qblk;            // CTAs per head
   int heads_per_group;   // causal launch order: heads whose query blocks interleave
-  float scale_log2;      // scale * log2(e)
+  float scale_log2;      // scale * log2(e) (e4m3: times the Q and K dequantisation scales)
+  float o_scale;         // e4m3: V's dequantisation scale (unused for bf16)
   // Split-KV: kv_splits CTAs share the key tiles of one query block; each
   // writes its normalised partial O (fp32 [kv_splits][BH][Nq][D]) and its
   // partial LSE (fp32 [kv_splits][BH][Nq], -inf when it saw no key) instead of
@@ -46,8 +47,14 @@ unsigned int* status_word();
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long timeout_ns,
                                  cudaStream_t stream);
 
+// Transposes e4m3 V [BH, N, d] into [BH, d, n_pad] (keys innermost) for the
+// e4m3 kernel's K-major P.V operand; keys in [N, n_pad) are written as zeros.
+cudaError_t launch_transpose_v8(const void* v, void* vt, long long BH, int N, int d, int n_pad,
+                                cudaStream_t stream);
+
 FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();
 FwdVariant fwd_variant_d256();
+FwdVariant fwd_variant_e4m3_d128();
 
 }  // namespace ea51

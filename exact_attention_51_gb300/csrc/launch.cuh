@@ -1,5 +1,6 @@
 // Kernel launch for one head dim (both causal flags).  Included by exactly one
-// translation unit per head dim so the three variants compile in parallel.
+// translation unit per head dim and input type so the variants compile in
+// parallel.
 #pragma once
 #include <atomic>
 
@@ -7,11 +8,11 @@
 
 namespace ea51 {
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const FwdParams& p, cudaStream_t stream) {
-  using L = Layout<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT>;
+  using L = Layout<D, F8>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8>;
   // The dynamic shared-memory opt-in is per device; remember which are done.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;

@@ -1,7 +1,7 @@
 // Thin inline-PTX wrappers for the sm_103a primitives the attention kernel
 // uses: mbarriers, TMA (cp.async.bulk.tensor), tensor memory (tcgen05.alloc /
-// ld / st), the 5th-generation tensor-core MMA (tcgen05.mma, kind::f16) and
-// the fences that order them.  Semantics follow the PTX ISA for sm_100-family
+// ld / st), the 5th-generation tensor-core MMA (tcgen05.mma, kind::f16 and
+// kind::f8f6f4) and the fences that order them.  Semantics follow the PTX ISA for sm_100-family
 // targets; nothing here is specific to attention.
 #pragma once
 #include <cstdint>
@@ -119,6 +119,13 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
                :
@@ -161,6 +168,24 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// kind::f8f6f4 forms of the two MMAs above (8-bit A and B, fp32 accumulate).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, i;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 i, %5, 0;\n\t"
+      "@i tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n\t.reg .pred p, i;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 i, %5, 0;\n\t"
+      "@i tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
 // Arrive once on `bar` when every earlier tcgen05.mma of the issuing lane is
 // done (only the lane with `issue` != 0 commits).
 __device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t issue) {
@@ -179,6 +204,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t issue) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A/B (format 0), fp32
+// accumulate, both operands K-major; same field positions as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -252,6 +283,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four fp32 values -> four e4m3 bytes (round to nearest even, saturating to
+// +-448), the first value in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float b0, float b1, float b2, float b3) {
+  uint32_t r;
+  // cvt packs its first source into the upper byte of each pair.
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(b0), "f"(b1), "f"(b2), "f"(b3));
   return r;
 }
 

@@ -127,3 +127,25 @@ def sample_rows(B: int, H: int, N: int, count: int, seed: int = 0, tile: int = 1
     while len(rows) < count:
         rows.add(int(torch.randint(0, BH * N, (1,), generator=g).item()))
     return sorted(rows)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 codes of a CPU tensor: ``(codes uint8, descale)`` with
+    descale the power of two 2^ceil(log2(amax / 448)), so that every
+    |x| / descale fits the format's largest finite value (448) and
+    ``descale * decode(codes)`` is the value the attention sees.  Rounding is
+    torch's round-to-nearest-even conversion to ``float8_e4m3fn``."""
+    amax = float(x.abs().max())
+    descale = 2.0 ** math.ceil(math.log2(amax / 448.0)) if amax > 0 else 1.0
+    codes = (x.float() / descale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), descale
+
+
+def make_inputs_e4m3(B: int, H: int, N: int, d: int, dist: str, seed: int,
+                     k_outlier_frac: float = 0.0):
+    """``make_inputs`` drawn the same way, then each tensor quantised to e4m3
+    with its own power-of-two scale: returns ``(q8, k8, v8, (sq, sk, sv))``
+    as uint8 CPU tensors and floats."""
+    q, k, v = make_inputs(B, H, N, d, dist, seed, k_outlier_frac)
+    (q8, sq), (k8, sk), (v8, sv) = (quantize_e4m3(t.float()) for t in (q, k, v))
+    return q8, k8, v8, (sq, sk, sv)

@@ -1,0 +1,62 @@
+/*
+ * exact_attention_51_gb300 -- C ABI of the 8-bit (e4m3) attention forward.
+ *
+ * The same exact attention as attn_fwd (include/attn_fwd.h), with Q, K and V
+ * given as OCP FP8 e4m3 codes and one dequantisation scale per tensor: the
+ * computed quantity is
+ *
+ *     O = softmax(scale * (sq Q8) (sk K8)^T [+ causal mask]) (sv V8),
+ *     LSE_i = log sum_j exp(scale * sq sk q8_i . k8_j)
+ *
+ * with sq, sk, sv the descale arguments and Q8, K8, V8 the decoded codes.
+ * The products run on the tensor cores' 8-bit path (tcgen05.mma
+ * kind::f8f6f4, fp32 accumulate).  P is rounded to e4m3 before P V (bf16 in
+ * attn_fwd), so O carries a relative rounding of up to 2^-4 per softmax
+ * weight; the running max, the row sum and LSE stay fp32.  The pages' FA-3
+ * thread (HN item 40939030) argues for adapting the kernel to the hardware it
+ * runs on; 8-bit operands at twice the bf16 tensor rate are that adaptation
+ * here -- the pages themselves give no FP8 algorithm.
+ */
+#ifndef EXACT_ATTENTION_51_GB300_ATTN_FP8_H
+#define EXACT_ATTENTION_51_GB300_ATTN_FP8_H
+
+#include <stddef.h>
+
+#include "attn_fwd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * e4m3 forward, Nq = Nk = N, d = 128.
+ *
+ *   q, k, v     e4m3 codes, one byte per element, [B,H,N,d] contiguous,
+ *               16-byte aligned; read only.
+ *   descale_q, descale_k, descale_v
+ *               finite and > 0: element x of Q means descale_q * e4m3(x).
+ *   o           written, bf16 [B,H,N,d], 16-byte aligned.
+ *   lse         written, fp32 [B,H,N] (natural log), 4-byte aligned.
+ *   scale       softmax scale (finite, >= 0), as in attn_fwd.
+ *   workspace   device buffer of attn_fwd_fp8_workspace_size(B, H, N, d)
+ *               bytes, 256-byte aligned: scratch for V transposed to
+ *               [B*H, d, round_up(N, 16)].  o, lse and workspace must not
+ *               overlap each other or q, k, v.
+ * Enqueues two kernels on `stream` (the V transpose, then the fused forward)
+ * and returns; status codes as in attn_fwd (d != 128, a non-positive or
+ * non-finite descale, a missing or short workspace: ATTN_ERR_INVALID_ARG).
+ */
+ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q,
+                          float descale_k, float descale_v, void* o, float* lse, int B, int H,
+                          int N, int d, float scale, int causal, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes for attn_fwd_fp8: B*H*d*round_up(N, 16), 256-byte padded
+ * (0 for invalid sizes or d != 128).  Host-only. */
+ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_51_GB300_ATTN_FP8_H */

@@ -82,6 +82,11 @@ def _bind(lib):
         lib.attn_bwd_ref_f64.restype = ctypes.c_int
         lib.attn_bwd_ref_bf16.argtypes = [_vp] * 7 + [_i64] * 4 + [_dbl, ctypes.c_int, ctypes.c_int]
         lib.attn_bwd_ref_bf16.restype = ctypes.c_int
+    lib.attn_ref_e4m3.argtypes = [_vp, _vp, _vp, _dbl, _dbl, _dbl, _i64, _i64, _i64, _i64,
+                                  _dbl, ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+    lib.attn_ref_e4m3.restype = ctypes.c_int
+    lib.attn_ref_e4m3_decode.argtypes = [ctypes.c_int]
+    lib.attn_ref_e4m3_decode.restype = _dbl
     lib.attn_ref_max_threads.argtypes = []
     lib.attn_ref_max_threads.restype = ctypes.c_int
     return lib
@@ -249,6 +254,55 @@ class Oracle:
         if rc:
             raise RuntimeError(f"oracle attn_ref_bf16_qk_rows failed: {rc}")
         return o[:R], lse[:R]
+
+
+    # -- e4m3 inputs with per-tensor dequantisation scales (attn_ref_e4m3)
+
+    def e4m3_decode(self, code: int) -> float:
+        """Value of one OCP e4m3 code (0..255) by the format's definition."""
+        return float(self.lib.attn_ref_e4m3_decode(int(code)))
+
+    def attn_e4m3(self, q, k, v, descale_q: float, descale_k: float, descale_v: float,
+                  causal: bool, scale: float, rows=None, nthreads: int = 0):
+        """e4m3 codes (uint8 numpy or torch uint8 / float8_e4m3fn CPU) [B,H,N,d]
+        -> (o fp64, lse fp64): whole tensors, or the listed flat rows
+        ((b*H+h)*N + i) as (o [R,d], lse [R])."""
+        qc, kc, vc = (_as_u8(t) for t in (q, k, v))
+        B, H, N, d = _shape4(qc)
+        if kc.shape != qc.shape or vc.shape != qc.shape:
+            raise ValueError("q, k, v must share one [B,H,N,d] shape")
+        if rows is None:
+            o = np.empty((B, H, N, d), np.float64)
+            lse = np.empty((B, H, N), np.float64)
+            rp, R = None, 0
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            R = rows.shape[0]
+            o = np.empty((max(R, 1), d), np.float64)
+            lse = np.empty((max(R, 1),), np.float64)
+            rp = rows.ctypes.data
+        rc = self.lib.attn_ref_e4m3(qc.ctypes.data, kc.ctypes.data, vc.ctypes.data,
+                                    float(descale_q), float(descale_k), float(descale_v),
+                                    B, H, N, d, float(scale), int(bool(causal)), rp, R,
+                                    o.ctypes.data, lse.ctypes.data, int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_e4m3 failed: {rc}")
+        return (o, lse) if rows is None else (o[:R], lse[:R])
+
+
+def _as_u8(t) -> np.ndarray:
+    """e4m3 codes as a contiguous uint8 numpy array (torch CPU tensors of
+    dtype uint8 or float8_e4m3fn are viewed, not converted)."""
+    if isinstance(t, np.ndarray):
+        if t.dtype != np.uint8:
+            raise TypeError("expected uint8 e4m3 codes")
+        return np.ascontiguousarray(t)
+    import torch
+    if t.device.type != "cpu":
+        raise TypeError("oracle inputs live on the CPU")
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("expected uint8 or float8_e4m3fn codes")
+    return t.contiguous().view(torch.uint8).numpy()
 
 
 def _qk_shapes(q, k, v):

@@ -29,8 +29,9 @@
  * has to agree with.
  *
  * Inputs are bf16 bit patterns (what the GPU reads) decoded here by a 16-bit
- * shift into the high half of an IEEE binary32, or plain fp64 arrays (used by
- * the pin tests).  Layout: contiguous [B,H,N,d] row-major for q, k, v, o and
+ * shift into the high half of an IEEE binary32, e4m3 codes with one
+ * dequantisation scale per tensor (decoded by the OCP 8-bit format's
+ * definition), or plain fp64 arrays (used by the pin tests).  Layout: contiguous [B,H,N,d] row-major for q, k, v, o and
  * [B,H,N] for lse.  All arithmetic is fp64 with libm exp/log.
  *
  * Parity status: pinned (tiled-vs-two-pass brute force, closed forms,
@@ -265,6 +266,93 @@ int attn_ref_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                   double *o, double *lse, int64_t B, int64_t H, int64_t N,
                   int64_t d, double scale, int causal, int nthreads) {
     return attn_ref_bf16_qk(q, k, v, o, lse, B, H, N, N, d, scale, causal, nthreads);
+}
+
+/* ---------------------------------------------------------------- e4m3 in */
+
+/*
+ * OCP 8-bit floating point (OFP8), E4M3 variant -> fp64: bit 7 sign, bits 6..3
+ * exponent (bias 7), bits 2..0 mantissa; exponent field 0 holds subnormals
+ * (m / 8) * 2^-6; exponent 15 with mantissa 7 is NaN; there are no infinities,
+ * so S.1111.110 = +-448 is the largest finite value.
+ */
+static double e4m3_to_f64(uint8_t c) {
+    const int e = (c >> 3) & 15, m = c & 7;
+    double x;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        x = ldexp((double)m / 8.0, -6);
+    else
+        x = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (c & 0x80) ? -x : x;
+}
+
+static void decode_head_e4m3(const uint8_t *src, double descale, double *dst, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) dst[t] = descale * e4m3_to_f64(src[t]);
+}
+
+/* Decodes one code (for the pin tests). */
+double attn_ref_e4m3_decode(int code) { return e4m3_to_f64((uint8_t)(code & 0xff)); }
+
+/*
+ * e4m3 inputs with per-tensor dequantisation scales, Nq = Nk = N: attention
+ * of (sq * Q8, sk * K8, sv * V8) by the same definition.  rows == NULL: every
+ * row, o [B,H,N,d] and lse [B,H,N]; else the nrows flat row ids (b*H + h)*N + i
+ * in rows[], results packed in o[r*d..] / lse[r] in that order.
+ */
+int attn_ref_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, double sq,
+                  double sk, double sv, int64_t B, int64_t H, int64_t N, int64_t d,
+                  double scale, int causal, const int64_t *rows, int64_t nrows,
+                  double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || (rows && nrows < 0)) return ORACLE_EINVAL;
+    int rc = check_sizes(B, H, N, N, d, causal);
+    if (rc) return rc;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= B * H * N) return ORACLE_EINVAL;
+    set_threads(nthreads);
+    const size_t elems = (size_t)N * (size_t)d;
+    const int64_t cap = rows ? (nrows ? nrows : 1) : 1;
+    double *Qh = (double *)malloc(elems * sizeof(double));
+    double *Kh = (double *)malloc(elems * sizeof(double));
+    double *Vh = (double *)malloc(elems * sizeof(double));
+    int64_t *sel = (int64_t *)malloc((size_t)cap * sizeof(int64_t));
+    int64_t *pos = (int64_t *)malloc((size_t)cap * sizeof(int64_t));
+    double *o_tmp = (double *)malloc((size_t)cap * (size_t)d * sizeof(double));
+    double *l_tmp = (double *)malloc((size_t)cap * sizeof(double));
+    if (!Qh || !Kh || !Vh || !sel || !pos || !o_tmp || !l_tmp) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    for (int64_t bh = 0; bh < B * H && rc == ORACLE_OK; ++bh) {
+        int64_t cnt = 0;
+        if (rows) {
+            for (int64_t r = 0; r < nrows; ++r)
+                if (rows[r] / N == bh) {
+                    sel[cnt] = rows[r] % N;
+                    pos[cnt] = r;
+                    ++cnt;
+                }
+            if (cnt == 0) continue;
+        }
+        decode_head_e4m3(q + bh * (int64_t)elems, sq, Qh, (int64_t)elems);
+        decode_head_e4m3(k + bh * (int64_t)elems, sk, Kh, (int64_t)elems);
+        decode_head_e4m3(v + bh * (int64_t)elems, sv, Vh, (int64_t)elems);
+        if (!rows) {
+            rc = head_rows(Qh, Kh, Vh, N, N, d, scale, causal, NULL, N,
+                           o + bh * (int64_t)elems, lse + bh * N);
+            continue;
+        }
+        rc = head_rows(Qh, Kh, Vh, N, N, d, scale, causal, sel, cnt, o_tmp, l_tmp);
+        for (int64_t t = 0; t < cnt && rc == ORACLE_OK; ++t) {
+            memcpy(o + pos[t] * d, o_tmp + t * d, (size_t)d * sizeof(double));
+            lse[pos[t]] = l_tmp[t];
+        }
+    }
+done:
+    free(Qh); free(Kh); free(Vh); free(sel); free(pos); free(o_tmp); free(l_tmp);
+    return rc;
 }
 
 /* Threads OpenMP will use for a parallel region (1 without OpenMP). */

@@ -397,12 +397,63 @@ def pin_rectangular_bf16_rows(orc):
     return fails
 
 
+def pin_e4m3_decode(orc):
+    """The e4m3 decoder against torch's float8_e4m3fn conversion (all 256
+    codes) and values the OCP 8-bit format fixes: 0x38 = 1, 0x7e = 448 (the
+    largest finite), 0x01 = 2^-9 (the smallest subnormal), 0x08 = 2^-6 (the
+    smallest normal), 0x80 = -0, 0x7f / 0xff = NaN."""
+    fails = []
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([orc.e4m3_decode(c) for c in range(256)])
+    nan_ok = np.isnan(ref) == np.isnan(got)
+    if not nan_ok.all() or not np.array_equal(ref[~np.isnan(ref)], got[~np.isnan(got)]):
+        bad = [c for c in range(256) if not (ref[c] == got[c] or (np.isnan(ref[c]) and np.isnan(got[c])))]
+        fails.append(f"e4m3 decode differs from torch at codes {bad[:8]}")
+    facts = {0x38: 1.0, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0x07: 7 * 2.0 ** -9,
+             0xB8: -1.0, 0x40: 2.0, 0x3C: 1.5}
+    for c, want in facts.items():
+        if orc.e4m3_decode(c) != want:
+            fails.append(f"e4m3 code {c:#04x} -> {orc.e4m3_decode(c)} (want {want})")
+    if not (orc.e4m3_decode(0x80) == 0.0 and np.signbit(orc.e4m3_decode(0x80))):
+        fails.append("e4m3 0x80 is not -0")
+    if not (np.isnan(orc.e4m3_decode(0x7F)) and np.isnan(orc.e4m3_decode(0xFF))):
+        fails.append("e4m3 0x7f / 0xff are not NaN")
+    return fails
+
+
+def pin_e4m3_attention(orc):
+    """Attention on e4m3 codes with per-tensor scales equals the fp64
+    attention of the dequantised tensors (torch's decoder times the scales),
+    whole and by rows."""
+    g = torch.Generator().manual_seed(8)
+    shp = (2, 2, 23, 16)
+    codes = []
+    for _ in range(3):
+        c = torch.randint(0, 256, shp, generator=g, dtype=torch.int64).to(torch.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x3A  # no NaN codes
+        codes.append(c)
+    q8, k8, v8 = codes
+    sc = (0.5, 0.125, 3.0)
+    deq = [c.view(torch.float8_e4m3fn).double().numpy() * s for c, s in zip(codes, sc)]
+    fails = []
+    rows = [0, 22, 23, 45, 91, 60]
+    for causal in (False, True):
+        o, lse = orc.attn_e4m3(q8, k8, v8, *sc, causal, 0.02)
+        o2, lse2 = orc.attn_f64(*deq, causal, 0.02)
+        fails += _close(f"e4m3 attention o causal={causal}", o, o2, 0.0)
+        fails += _close(f"e4m3 attention lse causal={causal}", lse, lse2, 0.0)
+        orow, lrow = orc.attn_e4m3(q8, k8, v8, *sc, causal, 0.02, rows=rows)
+        fails += _close(f"e4m3 rows o causal={causal}", orow, o.reshape(-1, 16)[rows], 0.0)
+        fails += _close(f"e4m3 rows lse causal={causal}", lrow, lse.reshape(-1)[rows], 0.0)
+    return fails
+
+
 ALL_PINS = [
     pin_online_softmax_tiling, pin_merge_law, pin_identity_values, pin_constant_values,
     pin_single_key, pin_uniform_queries, pin_zero_scale, pin_permutation,
     pin_causal_future_blind, pin_key_shift, pin_linearity_in_v, pin_library_sdpa,
     pin_golden, pin_bf16_decode, pin_rows_api, pin_bottom_right_suffix, pin_rectangular_sdpa,
-    pin_rectangular_bf16_rows,
+    pin_rectangular_bf16_rows, pin_e4m3_decode, pin_e4m3_attention,
 ]
 
 

@@ -209,3 +209,65 @@ def test_kvcache_split_heuristic(lib):
         B, H, N, d, c = args
         assert f(B, H, N, N, d, c, 152) == ea.attn_fwd_splitkv_num_splits(B, H, N, d, c, 152)
     assert f(1, 1, 9, 8, 128, True, 152) == 1  # invalid causal shape
+
+
+# ------------------------------------------------------------------- e4m3
+
+def _fp8(lib, p, ws, ws_bytes, d=128, descales=(1.0, 1.0, 1.0), N=256):
+    q, k, v, o, lse = p
+    return lib.attn_fwd_fp8(q, k, v, *descales, o, lse, 1, 2, N, d, 0.088, 1, ws, ws_bytes, None)
+
+
+def test_fp8_workspace_size(lib):
+    assert ea.attn_fwd_fp8_workspace_size(1, 2, 256, 128) == 2 * 128 * 256
+    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 128) == 256 * ((128 * 32 + 255) // 256)
+    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 64) == 0
+    assert ea.attn_fwd_fp8_workspace_size(0, 1, 17, 128) == 0
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    # every call below is invalid, so nothing is ever launched
+    p = ptrs(1 << 24)
+    need = ea.attn_fwd_fp8_workspace_size(1, 2, 256, 128)
+    ws = A + (1 << 30)
+    assert _fp8(lib, p, ws, need, d=64) == ea.ATTN_ERR_INVALID_ARG
+    for bad in [(0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, float("nan")),
+                (float("inf"), 1.0, 1.0)]:
+        assert _fp8(lib, p, ws, need, descales=bad) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, ws, need - 1) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, None, need) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, ws + 16, need) == ea.ATTN_ERR_MISALIGNED
+    assert _fp8(lib, p, ws, need, N=0) == ea.ATTN_ERR_INVALID_ARG
+    q, k, v, o, lse = p
+    assert _fp8(lib, [q + 8, k, v, o, lse], ws, need) == ea.ATTN_ERR_MISALIGNED
+    # o overlapping v (v spans 1*2*256*128 one-byte codes)
+    assert _fp8(lib, [q, k, v, v + 4096, lse], ws, need) == ea.ATTN_ERR_ALIAS
+    # the workspace overlapping q
+    assert _fp8(lib, p, q - (q % 256), need) == ea.ATTN_ERR_ALIAS
+
+
+# --------------------------------------------------------------- backward
+
+def test_bwd_rejects_bad_arguments(lib):
+    # every call below is invalid, so nothing is ever launched
+    N, d = 256, 64
+    n = 1 * 2 * N * d * 2
+    base = ptrs(1 << 24)
+    q, k, v, o, lse = base
+    g = A + 40 * (1 << 24)
+    dq, dk, dv = g + (1 << 24), g + 2 * (1 << 24), g + 3 * (1 << 24)
+    ws = g + 4 * (1 << 24)
+    need = ea.attn_bwd_workspace_size(1, 2, N)
+
+    def call(dd=d, w=ws, wb=need, grads=(dq, dk, dv), dout=g):
+        return lib.attn_bwd(q, k, v, o, dout, lse, *grads, 1, 2, N, dd, 0.125, 1, w, wb, None)
+
+    assert call(dd=256) == ea.ATTN_ERR_INVALID_ARG
+    assert call(wb=need - 1) == ea.ATTN_ERR_INVALID_ARG
+    assert call(w=None) == ea.ATTN_ERR_INVALID_ARG
+    assert call(w=ws + 16) == ea.ATTN_ERR_MISALIGNED
+    assert call(dout=None) == ea.ATTN_ERR_INVALID_ARG
+    assert call(grads=(dq + 2, dk, dv)) == ea.ATTN_ERR_MISALIGNED
+    assert call(grads=(dq, dq + n // 2, dv)) == ea.ATTN_ERR_ALIAS  # dk over dq
+    assert call(grads=(q, dk, dv)) == ea.ATTN_ERR_ALIAS  # dq over q
+    assert ea.attn_bwd_workspace_size(1, 2, 1) == 2 * 256 * ((2 * 128 * 4 + 255) // 256)

@@ -76,6 +76,13 @@ MUTANTS = [
     ("exp sign flipped", "s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
     ("max replaced by first score", "if (s[j] > m) m = s[j];", "if (j == 0) m = s[j];"),
     ("bf16 decode shift wrong", "((uint32_t)h) << 16;", "((uint32_t)h) << 15;"),
+    ("e4m3 exponent bias 8", "x = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "x = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3 subnormals scaled like normals", "x = ldexp((double)m / 8.0, -6);",
+     "x = ldexp((double)m / 8.0, -7);"),
+    ("e4m3 descale dropped", "dst[t] = descale * e4m3_to_f64(src[t]);",
+     "dst[t] = e4m3_to_f64(src[t]);"),
+    ("e4m3 sign ignored", "return (c & 0x80) ? -x : x;", "return x;"),
     ("dot product drops last feature", "for (int64_t c = 0; c < d; ++c) acc += q_i[c] * k_j[c];",
      "for (int64_t c = 0; c + 1 < d; ++c) acc += q_i[c] * k_j[c];"),
     ("q row of the wrong query", "attend_row(Qh + i * d,", "attend_row(Qh + (i > 0 ? i - 1 : 0) * d,"),
