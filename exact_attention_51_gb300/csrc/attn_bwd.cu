@@ -10,11 +10,13 @@
 //   preprocess  D and LSE * log2(e) per row into a padded workspace;
 //   dK/dV       one CTA per 128-key block: for every query block it
 //               recomputes S^T = K Q^T and dP^T = V dO^T in tensor memory,
-//               one thread per key row forms P^T and dS^T (bf16, written over
-//               the fp32 tiles), and the tensor core accumulates
+//               two threads per key row (one per half of the query block)
+//               form P^T and dS^T (bf16, written over the fp32 tiles), and
+//               the tensor core accumulates
 //               dV += P^T dO and dK += dS^T Q in tensor memory;
 //   dQ          one CTA per 128-query block: recomputes S and dP per key
-//               block, forms dS per query row, accumulates dQ += dS K.
+//               block, forms dS (two threads per query row), accumulates
+//               dQ += dS K.
 // S and dP are computed twice (once per kernel) so that no kernel needs a
 // transposed copy of dS or atomics: every MMA uses the operand layouts of the
 // forward kernel (K-major A/B from shared memory, or A from tensor memory
@@ -35,6 +37,17 @@ namespace {
 
 constexpr int BQ = 128;  // query rows per tile
 constexpr int BK = 128;  // key rows per tile
+// Warps: 0..7 elementwise (two per tensor-memory lane quadrant, each taking
+// half of the tile's 128 columns), 8 TMA, 9 MMA.
+constexpr int kComputeWarps = 8;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kBwdThreads = 320;
+// Packed bf16 output of column half h (64 fp32 columns at 64h -> 32 columns
+// of bf16 pairs at 64h): each 32-column chunk's 16 packed columns land on
+// columns this half has already read, never on the other half's.
+__host__ __device__ constexpr int packed_col(int h) { return 64 * h; }
+// tensor-memory column of the A operand (P^T, dS^T or dS) for K-step k
+__host__ __device__ constexpr int a_col(int k) { return k < 4 ? k * 8 : 64 + (k - 4) * 8; }
 
 template <int D>
 struct BwdLayout {
@@ -113,7 +126,7 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
 // ------------------------------------------------------------ dK / dV
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
@@ -137,11 +150,11 @@ __global__ void __launch_bounds__(256, 1)
   const int nq = nblk - q_first;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? 4u : 1u);
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? kComputeWarps : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       const uint32_t rb = bar(L::BAR_RES);
@@ -185,7 +198,7 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     const uint32_t leader = elect_one();
     constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);  // S^T, dP^T: both K-major
@@ -221,8 +234,8 @@ __global__ void __launch_bounds__(256, 1)
       for (int k = 0; k < BQ / 16; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
         const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-        mma_ts(tmem + L::ACC0, tmem + L::T1 + k * 8, oM + bo, kIdescTS, acc, leader);  // dV
-        mma_ts(tmem + L::ACC1, tmem + L::T2 + k * 8, qM + bo, kIdescTS, acc, leader);  // dK
+        mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), oM + bo, kIdescTS, acc, leader);  // dV
+        mma_ts(tmem + L::ACC1, tmem + L::T2 + a_col(k), qM + bo, kIdescTS, acc, leader);  // dK
       }
       mma_commit(bar(L::BAR_EMPTY + st), leader);
     }
@@ -232,11 +245,12 @@ __global__ void __launch_bounds__(256, 1)
       drain_phase(bar(L::BAR_DRAIN), 0u, w, kCodeDrain);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------- P^T, dS^T: one thread per key
-    const int r = warp * 32 + lane;  // key row in the block == TMEM lane
+  } else if (warp < kComputeWarps) {
+    // ---------------------- P^T, dS^T: one key row per thread, half the queries
+    const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column half
+    const int r = qd * 32 + lane;  // key row in the block == TMEM lane
     const int key = kb * 128 + r;
-    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lb = static_cast<uint32_t>(qd * 32) << 16;
     const float c = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < nq && ok; ++t) {
@@ -254,10 +268,11 @@ __global__ void __launch_bounds__(256, 1)
       const bool diag = CAUSAL && qblk == kb;     // key > query masked inside
       const bool tail = qblk * 128 + 128 > p.N;  // queries >= N masked
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        // chunk c2 of this half, then its packed result at packed_col(h) + 16 c2
         uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(tmem + lb + L::T1 + ch * 32, s);
-        tmem_ld_32x32b_x32(tmem + lb + L::T2 + ch * 32, dp);
+        tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + c2 * 32, s);
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + h * 64 + c2 * 32, dp);
         tmem_ld_wait(s);
         tmem_ld_wait(dp);
         uint32_t pk[16], dk[16];
@@ -265,20 +280,18 @@ __global__ void __launch_bounds__(256, 1)
         for (int e = 0; e < 16; ++e) {
           float pv[2], dv[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = ch * 32 + 2 * e + h;  // query within the block
-            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), c, -lse2[col]));
+          for (int u = 0; u < 2; ++u) {
+            const int col = h * 64 + c2 * 32 + 2 * e + u;  // query within the block
+            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + u]), c, -lse2[col]));
             if ((diag && key > qblk * 128 + col) || (tail && qblk * 128 + col >= p.N)) pp = 0.f;
-            pv[h] = pp;
-            dv[h] = pp * (__uint_as_float(dp[2 * e + h]) - dsm[col]);
+            pv[u] = pp;
+            dv[u] = pp * (__uint_as_float(dp[2 * e + u]) - dsm[col]);
           }
           pk[e] = pack_bf16x2(pv[0], pv[1]);
           dk[e] = pack_bf16x2(dv[0], dv[1]);
         }
-        // chunk ch's bf16 pairs land on columns 16ch..16ch+15, which belong
-        // to chunks already read (ch/2), never to one still to be read
-        tmem_st_32x32b_x16(tmem + lb + L::T1 + ch * 16, pk);
-        tmem_st_32x32b_x16(tmem + lb + L::T2 + ch * 16, dk);
+        tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, pk);
+        tmem_st_32x32b_x16(tmem + lb + L::T2 + packed_col(h) + c2 * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(256, 1)
         __nv_bfloat16* dst_row = (which == 0 ? p.dv : p.dk) + row * D;
         const float mul = which == 0 ? 1.f : p.scale;
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = h * (D / 64); ch < (h + 1) * (D / 64); ++ch) {
           uint32_t a[32];
           tmem_ld_32x32b_x32(tmem + lb + (which == 0 ? L::ACC0 : L::ACC1) + ch * 32, a);
           tmem_ld_wait(a);
@@ -315,7 +328,7 @@ __global__ void __launch_bounds__(256, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
@@ -324,7 +337,7 @@ __global__ void __launch_bounds__(256, 1)
 // ------------------------------------------------------------ dQ
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -348,11 +361,11 @@ __global__ void __launch_bounds__(256, 1)
   const int nk = CAUSAL ? qb + 1 : nblk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? 4u : 1u);
+    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? kComputeWarps : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     if (lane == 0) {
       const uint32_t rb = bar(L::BAR_RES);
       mbar_arrive_expect_tx(rb, 2 * L::TILE);
@@ -391,7 +404,7 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     const uint32_t leader = elect_one();
     constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);
@@ -424,8 +437,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int k = 0; k < BK / 16; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
-        mma_ts(tmem + L::ACC0, tmem + L::T1 + k * 8, kM + bo, kIdescTS, (t > 0 || k > 0) ? 1u : 0u,
-               leader);  // dQ += dS K
+        mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), kM + bo, kIdescTS,
+               (t > 0 || k > 0) ? 1u : 0u, leader);  // dQ += dS K
       }
       mma_commit(bar(L::BAR_EMPTY + st), leader);
     }
@@ -435,10 +448,11 @@ __global__ void __launch_bounds__(256, 1)
       drain_phase(bar(L::BAR_DRAIN), 0u, w, kCodeDrain);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    const int r = warp * 32 + lane;  // query row in the block == TMEM lane
+  } else if (warp < kComputeWarps) {
+    const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column half
+    const int r = qd * 32 + lane;  // query row in the block == TMEM lane
     const int qrow = qb * 128 + r;
-    const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lb = static_cast<uint32_t>(qd * 32) << 16;
     const float c = p.scale_log2;
     const size_t prow = static_cast<size_t>(bh) * p.Npad + qrow;
     const float l2 = p.lse2[prow];
@@ -454,10 +468,10 @@ __global__ void __launch_bounds__(256, 1)
       if (tail) lim = p.N - t * 128;
       if (diag) lim = min(lim, qrow - t * 128 + 1);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(tmem + lb + L::T1 + ch * 32, s);
-        tmem_ld_32x32b_x32(tmem + lb + L::T2 + ch * 32, dp);
+        tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + c2 * 32, s);
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + h * 64 + c2 * 32, dp);
         tmem_ld_wait(s);
         tmem_ld_wait(dp);
         uint32_t dk[16];
@@ -465,15 +479,15 @@ __global__ void __launch_bounds__(256, 1)
         for (int e = 0; e < 16; ++e) {
           float dv[2];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = ch * 32 + 2 * e + h;
-            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + h]), c, -l2));
+          for (int u = 0; u < 2; ++u) {
+            const int col = h * 64 + c2 * 32 + 2 * e + u;  // key within the block
+            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + u]), c, -l2));
             if ((diag || tail) && col >= lim) pp = 0.f;
-            dv[h] = pp * (__uint_as_float(dp[2 * e + h]) - dsum);
+            dv[u] = pp * (__uint_as_float(dp[2 * e + u]) - dsum);
           }
           dk[e] = pack_bf16x2(dv[0], dv[1]);
         }
-        tmem_st_32x32b_x16(tmem + lb + L::T1 + ch * 16, dk);
+        tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -486,7 +500,7 @@ __global__ void __launch_bounds__(256, 1)
       const bool valid = qrow < p.N;
       __nv_bfloat16* dst_row = p.dq + (static_cast<size_t>(bh) * p.N + (valid ? qrow : 0)) * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = h * (D / 64); ch < (h + 1) * (D / 64); ++ch) {
         uint32_t a[32];
         tmem_ld_32x32b_x32(tmem + lb + L::ACC0 + ch * 32, a);
         tmem_ld_wait(a);
@@ -505,7 +519,7 @@ __global__ void __launch_bounds__(256, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
@@ -525,9 +539,9 @@ cudaError_t launch_bwd_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
   if ((e = set_smem(bwd_dq_kernel<D, CAUSAL>, L::B_SMEM)) != cudaSuccess) return e;
   const unsigned nblk = static_cast<unsigned>((p.N + 127) / 128);
   const unsigned grid = nblk * static_cast<unsigned>(p.BH);
-  bwd_dkdv_kernel<D, CAUSAL><<<grid, 256, L::A_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
+  bwd_dkdv_kernel<D, CAUSAL><<<grid, kBwdThreads, L::A_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_dq_kernel<D, CAUSAL><<<grid, 256, L::B_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
+  bwd_dq_kernel<D, CAUSAL><<<grid, kBwdThreads, L::B_SMEM, stream>>>(*tq, *tk, *tv, *tdo, p);
   return cudaGetLastError();
 }
 
