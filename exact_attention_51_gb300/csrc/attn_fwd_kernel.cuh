@@ -36,10 +36,15 @@ namespace ea51 {
 
 constexpr int BM = 128;                      // query rows per tile (tcgen05 M)
 // log2 units: O and l are rescaled only when a row's max grows by more than
-// this; otherwise P keeps the old exponent offset (values up to 2^1).  A
-// larger threshold skips more rescales but lets a dominant weight be rounded
-// to bf16 (relative error up to 2^-8) where a fresh offset would make it 1.0.
-constexpr float kRescaleThreshold = 1.0f;
+// this; otherwise P keeps the old exponent offset (bf16 values up to 2^8).
+// A stale offset leaves a dominant weight at 2^x with x in (0, 8] instead of
+// exactly 1, so its rounding to bf16 (up to 2^-9 relative) would not cancel
+// against the fp32 normaliser; the softmax therefore gives O's normaliser
+// each tile's largest weight as rounded (see softmax_role).
+constexpr float kRescaleThreshold = 8.0f;
+// e4m3 P is 8 bits wide: a smaller threshold keeps small weights normal
+// numbers (see kF8Shift).
+constexpr float kRescaleThresholdF8 = 1.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
@@ -544,7 +549,12 @@ __device__ __forceinline__ float exp_store_f8(const uint32_t (&s)[NCH][32], int 
 // its values stay at or below 2^8 (e4m3 saturates at 448) and weights down to
 // 2^-13 of the row maximum stay normal numbers (3 mantissa bits).
 constexpr float kF8Shift = 7.0f;
-static_assert(kF8Shift + kRescaleThreshold <= 8.0f, "e4m3 P must stay below 448");
+static_assert(kF8Shift + kRescaleThresholdF8 <= 8.0f, "e4m3 P must stay below 448");
+
+// One weight rounded as the bf16 P stores it.
+__device__ __forceinline__ float round_bf16(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
 
 template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
@@ -567,6 +577,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   // exponent offset of P, O and l; l is the sum of the fp32 p.
   float m_used = 0.f;
   float l = 0.f;
+  float l_fix = 0.f;  // O's normaliser is l + l_fix (see below); LSE uses l
   if (n == 0) {
     // This split saw no key of this query tile: an empty partial.
     if (SPLIT && grow < p.Nq)
@@ -604,7 +615,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       m_used = (mx_c == -INFINITY) ? 0.f : mx_c;
     } else {
       const float m_new = fmaxf(m_used, mx_c);
-      const bool need = m_new > m_used + kRescaleThreshold;
+      const bool need = m_new > m_used + (F8 ? kRescaleThresholdF8 : kRescaleThreshold);
       if (__any_sync(0xffffffffu, need)) {
         // O holds PV(j-1) once o_done completes its phase j-1.
         ok = warp_wait_phase(bar(L::B_ODONE + q), static_cast<uint32_t>(j - 1) & 1u, w,
@@ -614,6 +625,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
         const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
         if (need) m_used = m_new;
         l *= alpha;
+        l_fix *= alpha;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t ov[32];
@@ -658,6 +670,18 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2 + (L::SPLIT_P ? 1 : 0)));
+
+    // l sums the fp32 weights while P.V uses them rounded.  O's normaliser
+    // takes the tile's largest weight (the one whose rounding error can be
+    // large next to l) as rounded, computed as exp_store computes it, so that
+    // a row dominated by one key gets that key's V back exactly; LSE keeps the
+    // unrounded sum.  Done after P is handed over, off the MMA's path.  The
+    // e4m3 path keeps its small threshold (a fresh offset makes the largest
+    // weight exact) and skips this.
+    if constexpr (!F8) {
+      const float pm = (mx == -INFINITY) ? 0.f : ex2_approx(fmaf(mx, c, -m_used));
+      l_fix += round_bf16(pm) - pm;
+    }
   }
 
   if (!ok) return;
@@ -670,7 +694,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   tc_fence_after_sync();
   // e4m3: O and l both carry the 2^kF8Shift factor; V's dequantisation
   // scale multiplies O.
-  const float inv_l = F8 ? p.o_scale / l : 1.f / l;
+  const float inv_l = F8 ? p.o_scale / (l + l_fix) : 1.f / (l + l_fix);
   const size_t row = static_cast<size_t>(t.bh) * p.Nq + (valid ? grow : 0);
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
   float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.Nq + row) * D;

@@ -159,6 +159,17 @@ def test_scale_values(scale):
         check_full(q, k, v, causal, scale=scale, label=f"scale={scale}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("scale", [0.5, 1.0])
+def test_peaked_rows_many_tiles(d, scale):
+    """Large scores over several key tiles: row maxima grow tile after tile
+    while the exponent offset stays stale (up to the rescale threshold), so
+    dominant weights are not exactly 1 when rounded into P."""
+    q, k, v = wl.make_inputs(1, 2, 1000, d, "normal", seed=int(scale * 10) + d)
+    for causal in (False, True):
+        check_full(q, k, v, causal, scale=scale, label=f"peaked scale={scale}")
+
+
 def test_outlier_keys_small():
     q, k, v = wl.make_inputs(1, 4, 1500, 128, "normal", seed=4321, k_outlier_frac=0.01)
     for causal in (False, True):
