@@ -64,9 +64,10 @@ struct BwdLayout {
   static constexpr int B_STAGE = 2 * TILE;
   static constexpr int B_OFF_BAR = B_OFF_RING + STAGES * B_STAGE;
   // barriers (both kernels): 0 resident-full, [1, 1+ST) ring full,
-  // [1+ST, 1+2ST) ring empty, s_full, p_ready, final, drain
+  // [1+ST, 1+2ST) ring empty, s_full[2 column halves], p_ready[2 halves],
+  // final, drain
   static constexpr int BAR_RES = 0, BAR_FULL = 1, BAR_EMPTY = 1 + STAGES, BAR_S = 1 + 2 * STAGES,
-                       BAR_P = BAR_S + 1, BAR_FINAL = BAR_P + 1, BAR_DRAIN = BAR_FINAL + 1,
+                       BAR_P = BAR_S + 2, BAR_FINAL = BAR_P + 2, BAR_DRAIN = BAR_FINAL + 1,
                        NBAR = BAR_DRAIN + 1;
   static constexpr int A_SMEM = A_OFF_BAR + NBAR * 8 + 8 + 1024;
   static constexpr int B_SMEM = B_OFF_BAR + NBAR * 8 + 8 + 1024;
@@ -144,13 +145,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // tile: key block kb of head bh; causal visits query blocks kb..nblk-1
   const int nblk = (p.N + 127) / 128;
-  const int bh = blockIdx.x / nblk;
-  const int kb = blockIdx.x % nblk;
+  // causal: key block kb visits nblk - kb query blocks, so blocks go out
+  // heaviest first across all heads (longest-processing-time order)
+  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % p.BH) : static_cast<int>(blockIdx.x / nblk);
+  const int kb = CAUSAL ? static_cast<int>(blockIdx.x / p.BH) : static_cast<int>(blockIdx.x % nblk);
   const int q_first = CAUSAL ? kb : 0;
   const int nq = nblk - q_first;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? kComputeWarps : 1u);
+    for (int i = 0; i < L::NBAR; ++i)
+      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps / 2 : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -201,43 +205,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     const uint32_t leader = elect_one();
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);  // S^T, dP^T: both K-major
-    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);     // dV, dK: B MN-major
+    // Work is split by query-column half: S^T and dP^T of block t+1 for the
+    // first 64 queries are computed while the elementwise warps of the second
+    // half still work on block t, so the tensor core keeps busy while each
+    // half forms its P^T and dS^T.
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 64, false);  // S^T, dP^T halves: K-major
+    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);    // dV, dK: B MN-major
     bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
     const uint64_t dK0 = sdesc_sw128(sbase + L::A_OFF_K, 16, 1024);
     const uint64_t dV0 = sdesc_sw128(sbase + L::A_OFF_V, 16, 1024);
-    for (int t = 0; t < nq && ok; ++t) {
-      const int st = t % L::STAGES;
-      ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
-                           kCodeMmaKV);
-      if (!ok) break;
-      const uint32_t base = sbase + L::A_OFF_RING + st * L::A_STAGE;
-      const uint64_t qK = sdesc_sw128(base, 16, 1024);                 // Q as K-major B
-      const uint64_t oK = sdesc_sw128(base + L::TILE, 16, 1024);       // dO as K-major B
-      const uint64_t qM = sdesc_sw128(base, L::PANEL, 1024);           // Q as MN-major B
-      const uint64_t oM = sdesc_sw128(base + L::TILE, L::PANEL, 1024); // dO as MN-major B
+    auto stage_base = [&](int t) {
+      return sbase + L::A_OFF_RING + static_cast<uint32_t>((t % L::STAGES) * L::A_STAGE);
+    };
+    auto wait_stage = [&](int t) {
+      return warp_wait_phase(bar(L::BAR_FULL + t % L::STAGES),
+                             static_cast<uint32_t>(t / L::STAGES) & 1u, w, kCodeMmaKV);
+    };
+    // S^T = K Q^T and dP^T = V dO^T of block t for queries [64 hh, 64 hh + 64)
+    auto issue_sdp = [&](int t, int hh) {
+      const uint32_t base = stage_base(t) + hh * 64 * 128;  // 64 rows into each 128-byte panel
+      const uint64_t qK = sdesc_sw128(base, 16, 1024);
+      const uint64_t oK = sdesc_sw128(base + L::TILE, 16, 1024);
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T1, dK0 + off, qK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // S^T
+        mma_ss(tmem + L::T1 + 64 * hh, dK0 + off, qK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T2, dV0 + off, oK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // dP^T
+        mma_ss(tmem + L::T2 + 64 * hh, dV0 + off, oK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
-      mma_commit(bar(L::BAR_S), leader);
-      ok = warp_wait_phase(bar(L::BAR_P), static_cast<uint32_t>(t) & 1u, w, kCodeMmaP);
-      if (!ok) break;
-      tc_fence_after_sync();
+      mma_commit(bar(L::BAR_S + hh), leader);
+    };
+    // dV += P^T dO and dK += dS^T Q over queries [64 hh, 64 hh + 64) of block t
+    auto issue_acc = [&](int t, int hh) {
+      const uint32_t base = stage_base(t);
+      const uint64_t qM = sdesc_sw128(base, L::PANEL, 1024);            // Q as MN-major B
+      const uint64_t oM = sdesc_sw128(base + L::TILE, L::PANEL, 1024);  // dO as MN-major B
 #pragma unroll
-      for (int k = 0; k < BQ / 16; ++k) {
+      for (int k = 4 * hh; k < 4 * hh + 4; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
         const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
         mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), oM + bo, kIdescTS, acc, leader);  // dV
         mma_ts(tmem + L::ACC1, tmem + L::T2 + a_col(k), qM + bo, kIdescTS, acc, leader);  // dK
       }
-      mma_commit(bar(L::BAR_EMPTY + st), leader);
+    };
+    if (ok && nq > 0) {
+      ok = wait_stage(0);
+      if (ok) {
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
+      }
+    }
+    for (int t = 0; t < nq && ok; ++t) {
+      const uint32_t ph = static_cast<uint32_t>(t) & 1u;
+      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_acc(t, 0);
+      if (t + 1 < nq) {
+        ok = wait_stage(t + 1);
+        if (!ok) break;
+        issue_sdp(t + 1, 0);  // over the first half's P^T / dS^T, read by the MMAs above
+      }
+      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_acc(t, 1);
+      mma_commit(bar(L::BAR_EMPTY + t % L::STAGES), leader);
+      if (t + 1 < nq) issue_sdp(t + 1, 1);
     }
     if (ok) mma_commit(bar(L::BAR_FINAL), leader);
     if (!ok) {
@@ -260,7 +297,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // too before reading them from shared memory
       ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
                            kCodeSoftS);
-      if (ok) ok = warp_wait_phase(bar(L::BAR_S), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      if (ok) ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
       if (!ok) break;
       tc_fence_after_sync();
       const float* lse2 = reinterpret_cast<const float*>(smem + L::A_OFF_RING + st * L::A_STAGE + 2 * L::TILE);
@@ -296,7 +333,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::BAR_P));
+      if (lane == 0) mbar_arrive(bar(L::BAR_P + h));
     }
     if (ok && nq > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
     if (ok) {
@@ -361,7 +398,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int nk = CAUSAL ? qb + 1 : nblk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < L::NBAR; ++i) mbar_init(bar(i), i == L::BAR_P ? kComputeWarps : 1u);
+    for (int i = 0; i < L::NBAR; ++i)
+      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps / 2 : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -406,41 +444,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     const uint32_t leader = elect_one();
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);
+    // Split by key-column half as in the dK/dV kernel: S and dP of block t+1
+    // for the first 64 keys overlap the second half's work on block t.
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 64, false);
     constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);
     bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
     const uint64_t qA = sdesc_sw128(sbase + L::B_OFF_Q, 16, 1024);
     const uint64_t oA = sdesc_sw128(sbase + L::B_OFF_DO, 16, 1024);
-    for (int t = 0; t < nk && ok; ++t) {
-      const int st = t % L::STAGES;
-      ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
-                           kCodeMmaKV);
-      if (!ok) break;
-      const uint32_t base = sbase + L::B_OFF_RING + st * L::B_STAGE;
+    auto stage_base = [&](int t) {
+      return sbase + L::B_OFF_RING + static_cast<uint32_t>((t % L::STAGES) * L::B_STAGE);
+    };
+    auto wait_stage = [&](int t) {
+      return warp_wait_phase(bar(L::BAR_FULL + t % L::STAGES),
+                             static_cast<uint32_t>(t / L::STAGES) & 1u, w, kCodeMmaKV);
+    };
+    // S = Q K^T and dP = dO V^T of key block t for keys [64 hh, 64 hh + 64)
+    auto issue_sdp = [&](int t, int hh) {
+      const uint32_t base = stage_base(t) + hh * 64 * 128;
       const uint64_t kK = sdesc_sw128(base, 16, 1024);
       const uint64_t vK = sdesc_sw128(base + L::TILE, 16, 1024);
-      const uint64_t kM = sdesc_sw128(base, L::PANEL, 1024);
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T1, qA + off, kK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // S
+        mma_ss(tmem + L::T1 + 64 * hh, qA + off, kK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T2, oA + off, vK + off, kIdescSS, k > 0 ? 1u : 0u, leader);  // dP
+        mma_ss(tmem + L::T2 + 64 * hh, oA + off, vK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
-      mma_commit(bar(L::BAR_S), leader);
-      ok = warp_wait_phase(bar(L::BAR_P), static_cast<uint32_t>(t) & 1u, w, kCodeMmaP);
-      if (!ok) break;
-      tc_fence_after_sync();
+      mma_commit(bar(L::BAR_S + hh), leader);
+    };
+    // dQ += dS K over keys [64 hh, 64 hh + 64) of block t
+    auto issue_dq = [&](int t, int hh) {
+      const uint64_t kM = sdesc_sw128(stage_base(t), L::PANEL, 1024);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
+      for (int k = 4 * hh; k < 4 * hh + 4; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
         mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), kM + bo, kIdescTS,
-               (t > 0 || k > 0) ? 1u : 0u, leader);  // dQ += dS K
+               (t > 0 || k > 0) ? 1u : 0u, leader);
       }
-      mma_commit(bar(L::BAR_EMPTY + st), leader);
+    };
+    if (ok && nk > 0) {
+      ok = wait_stage(0);
+      if (ok) {
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
+      }
+    }
+    for (int t = 0; t < nk && ok; ++t) {
+      const uint32_t ph = static_cast<uint32_t>(t) & 1u;
+      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_dq(t, 0);
+      if (t + 1 < nk) {
+        ok = wait_stage(t + 1);
+        if (!ok) break;
+        issue_sdp(t + 1, 0);
+      }
+      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);
+      if (!ok) break;
+      tc_fence_after_sync();
+      issue_dq(t, 1);
+      mma_commit(bar(L::BAR_EMPTY + t % L::STAGES), leader);
+      if (t + 1 < nk) issue_sdp(t + 1, 1);
     }
     if (ok) mma_commit(bar(L::BAR_FINAL), leader);
     if (!ok) {
@@ -459,7 +527,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float dsum = p.dsum[prow];
     bool ok = true;
     for (int t = 0; t < nk && ok; ++t) {
-      ok = warp_wait_phase(bar(L::BAR_S), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
       if (!ok) break;
       tc_fence_after_sync();
       const bool diag = CAUSAL && t == qb;
@@ -492,7 +560,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::BAR_P));
+      if (lane == 0) mbar_arrive(bar(L::BAR_P + h));
     }
     if (ok && nk > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
     if (ok) {
