@@ -4,7 +4,9 @@
                     [--workload long]
 
 One step = one ``attn_fwd`` call over one batch of the workload (the whole
-hot path: a single fused kernel).  The default workload is the long-sequence
+hot path: a single fused kernel).  ``--path fp8`` times ``attn_fwd_fp8`` on
+the workload's inputs quantised to e4m3, ``--path bwd`` times ``attn_bwd``
+(the same JSON line, with their own metric names).  The default workload is the long-sequence
 causal configuration the throughput target is stated on: B=1, H=32, N=16384,
 d=128, bf16, causal, Q,K,V ~ N(0,1) with 1% of the K rows scaled by 8.
 
@@ -82,6 +84,37 @@ def load_traffic(workload: str, causal: bool):
     if not e or e.get("kernel_source_sha") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ second bounds
+
+L2_BYTES = 129 * 1024 * 1024
+L2_FLUSH_BYTES = 256 * 1024 * 1024
+# Exponentials per clock per SM on GB300 (its special-function units run ex2
+# at twice the B200 rate); the unit count of the device, at the SM clock
+# sampled during the run, gives the second (ALU) bound of the softmax.
+EX2_PER_CLK_PER_SM = 32
+
+
+def percentiles(xs):
+    if not xs:
+        return None
+    ys = sorted(xs)
+    pick = lambda f: ys[min(len(ys) - 1, int(round(f * (len(ys) - 1))))]
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9), "n": len(ys)}
+
+
+def exp_bound(w, causal, ms, clocks, per_score=1.0):
+    """Exponentials per step (per_score per visible score) against the SFU
+    rate."""
+    import torch
+    exps = per_score * w.B * w.H * w.N * w.N * (0.5 if causal else 1.0)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = EX2_PER_CLK_PER_SM * sms * mhz * 1e6
+    achieved = exps / (ms * 1e-3)
+    return {"exps": exps, "achieved_per_s": achieved, "peak_per_s": peak, "frac": achieved / peak,
+            "peak_source": f"{EX2_PER_CLK_PER_SM} ex2/clk/SM x {sms} SMs x {mhz:.0f} MHz"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -260,6 +293,92 @@ def run_reference(args, w, causal):
     return 0
 
 
+class BenchPath:
+    """One benchmarked entry point: its host inputs (copied in every e2e
+    step), the device buffers of one step, the call, and its accounting."""
+
+    def __init__(self, name, metric, dtype, flops, launches, kernel, peak_mult, host_inputs,
+                 make_outputs, make_scratch, call, out_names):
+        self.name, self.metric, self.dtype = name, metric, dtype
+        self.flops, self.launches, self.kernel, self.peak_mult = flops, launches, kernel, peak_mult
+        self.host_inputs = host_inputs      # dict name -> CPU tensor
+        self.make_outputs = make_outputs    # dev -> dict name -> device tensor
+        self.make_scratch = make_scratch    # dev -> device scratch tensor or None
+        self.call = call                    # (inputs, outputs, scratch, stream) -> None
+        self.out_names = out_names          # outputs copied back in the e2e loop
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host_inputs.values())
+
+
+def make_path(args, w, causal, ea, dev):
+    import torch
+    scale = w.scale
+    if args.path == "fwd":
+        q, k, v = wl.workload_inputs(w)
+        splits = args.splits
+        if splits == 0:
+            splits = ea.attn_fwd_splitkv_num_splits(
+                w.B, w.H, w.N, w.d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)
+        ws_bytes = ea.attn_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, splits) if splits > 1 else 0
+
+        def call(i, o, scratch, st):
+            if splits > 1:
+                ea.attn_fwd_splitkv(i["q"], i["k"], i["v"], causal=causal, num_splits=splits,
+                                    out=o["o"], lse=o["lse"], workspace=scratch, stream=st)
+            else:
+                ea.attn_fwd(i["q"], i["k"], i["v"], causal=causal, out=o["o"], lse=o["lse"], stream=st)
+        p = BenchPath("fwd", METRIC, "bf16", w.flops(causal), 2 if splits > 1 else 1,
+                      f"attn_fwd_kernel<{w.d},{str(causal).lower()}>", 1.0,
+                      {"q": q, "k": k, "v": v},
+                      lambda d: {"o": torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=d),
+                                 "lse": torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=d)},
+                      lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
+                      call, ["o", "lse"])
+        p.splits = splits
+        return p
+    if args.path == "fp8":
+        q8, k8, v8, sc = wl.make_inputs_e4m3(w.B, w.H, w.N, w.d, w.dist, w.seed, w.k_outlier_frac)
+        ws_bytes = ea.attn_fwd_fp8_workspace_size(w.B, w.H, w.N, w.d)
+
+        def call(i, o, scratch, st):
+            ea.attn_fwd_fp8(i["q"], i["k"], i["v"], *sc, causal=causal, out=o["o"], lse=o["lse"],
+                            workspace=scratch, stream=st)
+        p = BenchPath("fp8", "attention fwd TFLOP/s (e4m3 Q/K/V, per-tensor scales) and % of "
+                      "GB300 dense FP8 peak", "e4m3", w.flops(causal), 2,
+                      f"attn_fwd_kernel<{w.d},{str(causal).lower()},e4m3> + V transpose",
+                      2.0,  # dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s nominal)
+                      {"q": q8, "k": k8, "v": v8},
+                      lambda d: {"o": torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=d),
+                                 "lse": torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=d)},
+                      lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
+                      call, ["o", "lse"])
+        p.splits = 1
+        return p
+    # backward: Q, K, V, the forward's O and LSE, and dO are the inputs
+    q, k, v = wl.workload_inputs(w)
+    g = wl.make_inputs(w.B, w.H, w.N, w.d, w.dist, w.seed + 500)[0]
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o, lse = ea.attn_fwd(qd, kd, vd, causal=causal)
+    o_h, lse_h = o.cpu(), lse.cpu()
+    del qd, kd, vd, o, lse
+    ws_bytes = ea.attn_bwd_workspace_size(w.B, w.H, w.N)
+
+    def call(i, o, scratch, st):
+        ea.attn_bwd(i["q"], i["k"], i["v"], i["o"], i["lse"], i["do"], causal=causal,
+                    dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=scratch, stream=st)
+    p = BenchPath("bwd", "attention bwd TFLOP/s (bf16; 2.5x the forward's algorithmic FLOPs) and % "
+                  "of GB300 dense BF16 peak", "bf16", 2.5 * w.flops(causal), 3,
+                  "attn_bwd: row statistics + dK/dV + dQ kernels", 1.0,
+                  {"q": q, "k": k, "v": v, "o": o_h, "lse": lse_h, "do": g},
+                  lambda d: {n: torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=d)
+                             for n in ("dq", "dk", "dv")},
+                  lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
+                  call, ["dq", "dk", "dv"])
+    p.splits = 1
+    return p
+
+
 def run_ours(args, w, causal):
     import torch
     import torch.distributed as dist
@@ -275,71 +394,89 @@ def run_ours(args, w, causal):
     eabuild.build()
     ea.load_library()
 
-    q_h, k_h, v_h = wl.workload_inputs(w)
-    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    flops = w.flops(causal)
+    path = make_path(args, w, causal, ea, dev)
+    ins = {n: t.to(dev) for n, t in path.host_inputs.items()}
+    outs = path.make_outputs(dev)
+    scratch = path.make_scratch(dev)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
         if ws > 1:
             dist.barrier()
 
+    def step(st=None):
+        path.call(ins, outs, scratch, st)
+
     # ---- device-resident timing
-    splits = args.splits
-    if splits == 0:
-        splits = ea.attn_fwd_splitkv_num_splits(
-            w.B, w.H, w.N, w.d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)
-    ws_bytes = ea.attn_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, splits) if splits > 1 else 0
-    workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-
-    def fwd(qq, kk, vv, oo, ll, st=None):
-        if splits > 1:
-            ea.attn_fwd_splitkv(qq, kk, vv, causal=causal, num_splits=splits, out=oo, lse=ll,
-                                workspace=workspace, stream=st)
-        else:
-            ea.attn_fwd(qq, kk, vv, causal=causal, out=oo, lse=ll, stream=st)
-
     for _ in range(args.warmup):
-        fwd(q, k, v, o, lse)
+        step()
     torch.cuda.synchronize(dev)
     st, detail = ea.attn_fwd_device_status()
     if st != ea.ATTN_OK:
         raise RuntimeError(f"device wait timed out during warm-up (code {detail:#x})")
 
+    # Inputs and outputs smaller than twice L2 would be served from L2 on
+    # repeated launches: then every step is timed on its own, after a write
+    # of L2_FLUSH_BYTES that evicts them.
+    io_bytes = path.h2d_bytes() + sum(t.numel() * t.element_size() for t in outs.values())
+    flush = io_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
     sampler = ClockSampler(gpu_id_for(local))
     time.sleep(0.3)  # let nvidia-smi start printing
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per_step = []
     barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.monotonic()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        fwd(q, k, v, o, lse)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush_buf.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        per_step = [a.elapsed_time(b) for a, b in evs]
+        ms = sum(per_step) / len(per_step)
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = ev0.elapsed_time(ev1) / args.steps
     t_host1 = time.monotonic()
     barrier()
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
-    ms = ev0.elapsed_time(ev1) / args.steps
+    if not flush:
+        # step-by-step spread, outside the timed region above
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(min(args.steps, 50))]
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        per_step = [a.elapsed_time(b) for a, b in evs]
+    del flush_buf
     st, detail = ea.attn_fwd_device_status()
     if st != ea.ATTN_OK:
         raise RuntimeError(f"device wait timed out in the timed region (code {detail:#x})")
 
     # ---- end to end: pinned host buffers, copies inside the timed region.
     # Two device buffer sets; step i copies its inputs in on an H2D stream,
-    # computes on the compute stream and copies O and LSE out on a D2H stream,
-    # so the copies of one step overlap the kernel of the neighbouring steps
-    # (the copy engines and the SMs are separate hardware).
-    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-    op = [torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    lp = [torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory() for _ in range(2)]
-    bufs = [dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
-                 o=torch.empty_like(q), l=torch.empty_like(lse)) for _ in range(2)]
-    del o, lse, q, k, v
+    # computes on the compute stream and copies the results out on a D2H
+    # stream, so the copies of one step overlap the kernels of the
+    # neighbouring steps (the copy engines and the SMs are separate hardware).
+    pinned = {n: t.pin_memory() for n, t in path.host_inputs.items()}
+    back = [{n: torch.empty(outs[n].shape, dtype=outs[n].dtype).pin_memory() for n in path.out_names}
+            for _ in range(2)]
+    bufs = [dict(ins={n: torch.empty_like(t) for n, t in ins.items()}, outs=path.make_outputs(dev),
+                 scratch=path.make_scratch(dev)) for _ in range(2)]
+    del ins, outs, scratch
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -351,17 +488,16 @@ def run_ours(args, w, causal):
         b = bufs[i % 2]
         s_h2d.wait_event(ev_free[i % 2])
         with torch.cuda.stream(s_h2d):
-            b["q"].copy_(qp, non_blocking=True)
-            b["k"].copy_(kp, non_blocking=True)
-            b["v"].copy_(vp, non_blocking=True)
+            for n, t in pinned.items():
+                b["ins"][n].copy_(t, non_blocking=True)
             ev_in[i % 2].record(s_h2d)
         stream.wait_event(ev_in[i % 2])
-        fwd(b["q"], b["k"], b["v"], b["o"], b["l"], stream)
+        path.call(b["ins"], b["outs"], b["scratch"], stream)
         ev_done[i % 2].record(stream)
         s_d2h.wait_event(ev_done[i % 2])
         with torch.cuda.stream(s_d2h):
-            op[i % 2].copy_(b["o"], non_blocking=True)
-            lp[i % 2].copy_(b["l"], non_blocking=True)
+            for n in path.out_names:
+                back[i % 2][n].copy_(b["outs"][n], non_blocking=True)
             ev_free[i % 2].record(s_d2h)
 
     for i in range(max(1, min(args.warmup, 3))):
@@ -380,47 +516,61 @@ def run_ours(args, w, causal):
     st, detail = ea.attn_fwd_device_status()
     if st != ea.ATTN_OK:
         raise RuntimeError(f"device wait timed out in the end-to-end loop (code {detail:#x})")
-    h2d = 3 * q_h.numel() * 2
-    d2h = q_h.numel() * 2 + w.B * w.H * w.N * 4
+    h2d = path.h2d_bytes()
+    d2h = sum(back[0][n].numel() * back[0][n].element_size() for n in path.out_names)
 
     # ---- max over ranks
     ms, e2e_ms = reduce_max_over_ranks([ms, e2e_ms], dev)
 
     if rank == 0:
         peaks, peak_src = load_peaks()
-        achieved = flops / (ms * 1e-3) / 1e12
-        traffic = load_traffic(args.workload, causal)
+        peak = peaks["bf16_tflops"] * path.peak_mult
+        achieved = path.flops / (ms * 1e-3) / 1e12
+        traffic = load_traffic(args.workload, causal) if path.name == "fwd" else None
+        q_bytes = w.B * w.H * w.N * w.d * 2
         line = {
-            "metric": METRIC,
-            "value": whole_job_tflops(flops, ws, ms),
+            "metric": path.metric,
+            "value": whole_job_tflops(path.flops, ws, ms),
             "unit": "TFLOP/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": path.dtype,
             "data": "synthetic",
             "config": {"workload": w.describe(causal), "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                       "causal": causal, "scale": w.scale,
-                       "l2": "inputs larger than L2 (3 x %d MiB bf16), no flush" % (
-                           q_h.numel() * 2 >> 20),
+                       "causal": causal, "scale": w.scale, "path": path.name,
+                       "l2": ("L2 flushed (%d MiB write) before each step; per-step CUDA "
+                              "events" % (L2_FLUSH_BYTES >> 20)) if flush else
+                             ("inputs larger than L2 (3 x %d MiB bf16), no flush" % (q_bytes >> 20)),
                        "parallelism": f"replicas x{ws} (independent batches, no collective)",
-                       "kv_splits": splits},
-            "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
-                         "kernel": f"attn_fwd_kernel<{w.d},{str(causal).lower()}>"},
+                       "kv_splits": path.splits},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst" + (
+                             " x 2 (nominal fp8 : bf16 rate)" if path.peak_mult == 2.0 else ""),
+                         "kernel": path.kernel},
+            "latency_ms": percentiles(per_step),
+            "exp_bound": exp_bound(w, causal, ms, clocks, 2.0 if path.name == "bwd" else 1.0),
+            "hbm": {"min_bytes": w.min_hbm_bytes(),
+                    "achieved_gbs": w.min_hbm_bytes() / (ms * 1e-3) / 1e9,
+                    "frac": w.min_hbm_bytes() / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "peak_source": f"{peak_src} copy"} if path.name == "fwd" else None,
             "clocks": clocks,
-            "e2e": {"value": whole_job_tflops(flops, ws, e2e_ms), "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_tflops(path.flops, ws, e2e_ms), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
-                    "how": "pinned host buffers; H2D, kernel and D2H on three streams, "
+                    "how": "pinned host buffers; H2D, kernels and D2H on three streams, "
                            "double-buffered across steps"},
-            "gpu_launches": args.steps * (2 if splits > 1 else 1),
+            "gpu_launches": args.steps * path.launches,
         }
-        if ws == 1 and not args.no_cpu_baseline:
+        if path.name == "fwd":
+            line["pct_of_bf16_peak"] = line["pct_of_peak"]
+        if ws == 1 and not args.no_cpu_baseline and path.name == "fwd":
+            q_h, k_h, v_h = (path.host_inputs[n] for n in ("q", "k", "v"))
             tf, secs, nrows, cores = time_oracle(w, causal, q_h, k_h, v_h, args.cpu_seconds, 99)
             line["cpu_baseline"] = {
                 "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -442,6 +592,9 @@ def main(argv=None):
     ap.add_argument("--causal", choices=["default", "0", "1"], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fwd", "fp8", "bwd"], default="fwd",
+                    help="fwd: attn_fwd (bf16, the headline); fp8: attn_fwd_fp8 on the "
+                         "workload's inputs quantised to e4m3; bwd: attn_bwd")
     ap.add_argument("--splits", type=int, default=1,
                     help="1: attn_fwd; >1: attn_fwd_splitkv with that many key splits; "
                          "0: attn_fwd_splitkv with its default split count")
@@ -450,7 +603,13 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     w = wl.WORKLOADS[args.workload]
     causal = w.causal[-1] if args.causal == "default" else args.causal == "1"
+    if args.path == "fp8" and w.d != 128:
+        ap.error("--path fp8 needs a d = 128 workload")
+    if args.path == "bwd" and w.d not in (64, 128):
+        ap.error("--path bwd needs a d = 64 or 128 workload")
     if args.impl == "reference":
+        if args.path != "fwd":
+            ap.error("--impl reference times the forward oracle only")
         return run_reference(args, w, causal)
     return run_ours(args, w, causal)
 
