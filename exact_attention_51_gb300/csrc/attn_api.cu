@@ -503,6 +503,13 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.N = N;
   p.Npad = npad;
   p.BH = static_cast<int>(BH);
+  {
+    // each CTA streams two [N, d] bf16 operands of its head (Q and dO, or K
+    // and V): group as many heads as keep them within about half of L2
+    const double per_head = 2.0 * N * d * 2;
+    const int64_t g = static_cast<int64_t>((64.0 * 1024 * 1024) / per_head);
+    p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  }
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   const cudaError_t e = ea51::launch_bwd(&tq, &tk, &tv, &tdo, p, o, dout, lse, d, causal != 0,

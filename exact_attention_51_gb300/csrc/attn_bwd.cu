@@ -77,6 +77,19 @@ struct BwdLayout {
   static_assert(A_SMEM <= 232448 && B_SMEM <= 232448, "shared memory");
 };
 
+// Causal CTA order: heaviest blocks first (longest-processing-time order)
+// across a group of heads_per_group heads whose streamed operands fit in
+// about half of L2; `heavy_rank` 0 is the heaviest block of a head.
+__device__ __forceinline__ void grouped_order(int cta, int nblk, int BH, int hpg, int& bh,
+                                              int& heavy_rank) {
+  const int per_group = hpg * nblk;
+  const int group = cta / per_group;
+  const int gs = min(hpg, BH - group * hpg);
+  const int within = cta - group * per_group;
+  bh = group * hpg + within % gs;
+  heavy_rank = within / gs;
+}
+
 struct BwdTile {
   int bh, blk, n;  // head, this CTA's block, number of blocks it visits
   int first;       // first visited block of the other operand
@@ -145,10 +158,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // tile: key block kb of head bh; causal visits query blocks kb..nblk-1
   const int nblk = (p.N + 127) / 128;
-  // causal: key block kb visits nblk - kb query blocks, so blocks go out
-  // heaviest first across all heads (longest-processing-time order)
-  const int bh = CAUSAL ? static_cast<int>(blockIdx.x % p.BH) : static_cast<int>(blockIdx.x / nblk);
-  const int kb = CAUSAL ? static_cast<int>(blockIdx.x / p.BH) : static_cast<int>(blockIdx.x % nblk);
+  // causal: key block kb visits nblk - kb query blocks (heaviest: kb = 0)
+  int bh, kb;
+  if (CAUSAL) {
+    grouped_order(static_cast<int>(blockIdx.x), nblk, p.BH, p.heads_per_group, bh, kb);
+  } else {
+    bh = static_cast<int>(blockIdx.x) / nblk;
+    kb = static_cast<int>(blockIdx.x) % nblk;
+  }
   const int q_first = CAUSAL ? kb : 0;
   const int nq = nblk - q_first;
 
@@ -393,8 +410,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // tile: query block qb of head bh (heaviest first when causal); visits key
   // blocks 0..qb (causal) or all
   const int nblk = (p.N + 127) / 128;
-  const int bh = blockIdx.x % p.BH;
-  const int qb = CAUSAL ? nblk - 1 - static_cast<int>(blockIdx.x / p.BH) : static_cast<int>(blockIdx.x / p.BH);
+  int bh, qb;
+  if (CAUSAL) {
+    int rank;
+    grouped_order(static_cast<int>(blockIdx.x), nblk, p.BH, p.heads_per_group, bh, rank);
+    qb = nblk - 1 - rank;
+  } else {
+    // a head's blocks next to each other, so its K and V stay in L2
+    bh = static_cast<int>(blockIdx.x) / nblk;
+    qb = static_cast<int>(blockIdx.x) % nblk;
+  }
   const int nk = CAUSAL ? qb + 1 : nblk;
 
   if (threadIdx.x == 0) {

@@ -16,6 +16,7 @@ struct BwdParams {
   int N;
   int Npad;              // N rounded up to 128
   int BH;
+  int heads_per_group;   // causal launch order: heads whose blocks interleave
   float scale;
   float scale_log2;      // scale * log2(e)
 };
