@@ -106,3 +106,41 @@ def test_backward_sums():
         sg = g.double().sum(2)
         assert (sv - sg).abs().max().item() <= 0.05 * sg.abs().max().item() + 0.05
         assert dk.double().sum(2).abs().max().item() <= 0.05 * dk.double().abs().sum(2).max().item()
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_backward_full_size_sampled_heads(causal):
+    """The mid workload (B=4 H=16 N=4096 d=128) in one call; two heads
+    compared whole against the fp64 oracle run on those heads alone."""
+    w = wl.WORKLOADS["mid"]
+    q, k, v = wl.workload_inputs(w)
+    g = wl.make_inputs(w.B, w.H, w.N, w.d, w.dist, w.seed + 500)[0]
+    qd, kd, vd, gd = (t.cuda() for t in (q, k, v, g))
+    o, lse = ea.attn_fwd(qd, kd, vd, causal=causal)
+    dq, dk, dv = ea.attn_bwd(qd, kd, vd, o, lse, gd, causal=causal)
+    st, detail = ea.attn_fwd_device_status()
+    assert st == ea.ATTN_OK, f"device-side wait timed out (code {detail:#x})"
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+        ref = orc().attn_bwd_bf16(sl(q), sl(k), sl(v), sl(g), causal, w.scale)
+        got = [sl(t).float().cpu().numpy() for t in (dq, dk, dv)]
+        msgs = check(got, ref, f"mid head ({b},{h}) causal={causal}")
+        assert not msgs, "\n".join(msgs)
+
+
+def test_backward_long_column_sums():
+    """The long workload (B=1 H=32 N=16384, 1% of K rows x8), causal, in one
+    call; properties that hold at any size: per head, sum_j dV_j = sum_i dO_i
+    and sum_j dK_j = 0 (softmax rows sum to one), up to bf16 rounding."""
+    w = wl.WORKLOADS["long"]
+    q, k, v = (t.cuda() for t in wl.workload_inputs(w))
+    g = wl.make_inputs(w.B, w.H, w.N, w.d, w.dist, w.seed + 500)[0].cuda()
+    o, lse = ea.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = ea.attn_bwd(q, k, v, o, lse, g, causal=True)
+    st, detail = ea.attn_fwd_device_status()
+    assert st == ea.ATTN_OK, f"device-side wait timed out (code {detail:#x})"
+    assert bool(torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all())
+    sv, sg = dv.double().sum(2), g.double().sum(2)
+    assert (sv - sg).abs().max().item() <= 0.02 * sg.abs().max().item() + 0.5
+    sk = dk.double().sum(2)
+    assert sk.abs().max().item() <= 0.02 * dk.double().abs().sum(2).max().item()
