@@ -603,8 +603,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     w = wl.WORKLOADS[args.workload]
     causal = w.causal[-1] if args.causal == "default" else args.causal == "1"
-    if args.path == "fp8" and w.d != 128:
-        ap.error("--path fp8 needs a d = 128 workload")
+    if args.path == "fp8" and w.d not in (128, 256):
+        ap.error("--path fp8 needs a d = 128 or 256 workload")
     if args.path == "bwd" and w.d not in (64, 128):
         ap.error("--path bwd needs a d = 64 or 128 workload")
     if args.impl == "reference":

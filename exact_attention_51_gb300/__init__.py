@@ -172,7 +172,7 @@ def attn_fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def attn_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
                  causal: bool = False, scale: float | None = None, out=None, lse=None,
                  workspace=None, stream=None):
-    """Attention forward on e4m3 inputs: q, k, v CUDA tensors [B, H, N, 128]
+    """Attention forward on e4m3 inputs: q, k, v CUDA tensors [B, H, N, d], d = 128 or 256,
     of dtype float8_e4m3fn (or uint8 holding e4m3 codes), element x meaning
     ``descale * x``.  Returns ``(o, lse)``: o bf16 [B,H,N,d], lse fp32
     [B,H,N].  The V-transpose workspace is allocated with torch unless

@@ -386,7 +386,7 @@ int attn_fwd_device_status(void* stream, unsigned int* detail) {
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
 
 size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || d != 128) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return 0;
   const size_t n_pad = (static_cast<size_t>(N) + 15) / 16 * 16;
   return align256(static_cast<size_t>(B) * H * d * n_pad);
 }
@@ -395,7 +395,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
                  float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
                  int causal, void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || d != 128) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   for (const float ds : {descale_q, descale_k, descale_v})
     if (!std::isfinite(ds) || ds <= 0.f) return ATTN_ERR_INVALID_ARG;
@@ -424,7 +424,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
   const int n_pad = (N + 15) / 16 * 16;
   cudaError_t e = ea51::launch_transpose_v8(v, workspace, BH, N, d, n_pad, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  const ea51::FwdVariant var = ea51::fwd_variant_e4m3_d128();
+  const ea51::FwdVariant var = d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
   alignas(64) CUtensorMap tq, tk, tv;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if ((rc = encode_tiled(&tq, q, u8, 1, BH, N, d, d, 128)) != ATTN_OK) return rc;

@@ -1,21 +1,22 @@
-// e4m3 (8-bit) inputs, head dim 128: the fused forward with Q K^T and P V on
-// tcgen05.mma kind::f8f6f4, and the V transpose it reads its P.V operand from.
+// e4m3 (8-bit) inputs, head dims 128 and 256: the fused forward with Q K^T
+// and P V on tcgen05.mma kind::f8f6f4, and the V transpose it reads its P.V
+// operand from.
 #include "launch.cuh"
 
 namespace ea51 {
 
 namespace {
 
-// One CTA moves 128 keys x 128 columns of one head: coalesced 16-byte loads
-// of V rows into shared memory, then 16-byte stores of 16 consecutive keys of
-// one column of V^T.  Keys in [N, n_pad) are written as zeros.
+// One CTA moves 128 keys x kTCols columns of one head: coalesced 16-byte
+// loads of V rows into shared memory, then 16-byte stores of 16 consecutive
+// keys of one column of V^T.  Keys in [N, n_pad) are written as zeros.
 constexpr int kTKeys = 128;
-constexpr int kTCols = 128;
-constexpr int kTPitch = kTCols + 4;  // bytes per staged row (breaks bank alignment)
 
+template <int kTCols>
 __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __restrict__ v,
                                                            uint8_t* __restrict__ vt, int N,
                                                            int n_pad, int nblk) {
+  constexpr int kTPitch = kTCols + 4;  // bytes per staged row (breaks bank alignment)
   __shared__ __align__(16) uint8_t tile[kTKeys * kTPitch];
   const int key0 = static_cast<int>(blockIdx.x % static_cast<unsigned>(nblk)) * kTKeys;
   const size_t bh = blockIdx.x / static_cast<unsigned>(nblk);
@@ -52,11 +53,12 @@ __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __rest
   }
 }
 
+template <int D>
 cudaError_t launch_e4m3(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                         const FwdParams& p, bool causal, cudaStream_t stream) {
   if (p.kv_splits != 1) return cudaErrorInvalidValue;
-  return causal ? launch_one<128, true, false, true>(tq, tk, tv, p, stream)
-                : launch_one<128, false, false, true>(tq, tk, tv, p, stream);
+  return causal ? launch_one<D, true, false, true>(tq, tk, tv, p, stream)
+                : launch_one<D, false, false, true>(tq, tk, tv, p, stream);
 }
 
 }  // namespace
@@ -64,16 +66,27 @@ cudaError_t launch_e4m3(const CUtensorMap* tq, const CUtensorMap* tk, const CUte
 cudaError_t launch_transpose_v8(const void* v, void* vt, long long BH, int N, int d, int n_pad,
                                 cudaStream_t stream) {
   const long long nblk = (static_cast<long long>(N) + kTKeys - 1) / kTKeys;
-  if (d != kTCols || N < 1 || n_pad % 16 != 0 || n_pad < N || BH < 1 || BH * nblk > 0x7fffffffLL)
+  if ((d != 128 && d != 256) || N < 1 || n_pad % 16 != 0 || n_pad < N || BH < 1 ||
+      BH * nblk > 0x7fffffffLL)
     return cudaErrorInvalidValue;
-  transpose_v8_kernel<<<static_cast<unsigned>(BH * nblk), 256, 0, stream>>>(
-      static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
+  const unsigned grid = static_cast<unsigned>(BH * nblk);
+  if (d == 128)
+    transpose_v8_kernel<128><<<grid, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
+  else
+    transpose_v8_kernel<256><<<grid, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
   return cudaGetLastError();
 }
 
 FwdVariant fwd_variant_e4m3_d128() {
   using L = Layout<128, true>;
-  return FwdVariant{L::BN, L::NQ * BM, &launch_e4m3};
+  return FwdVariant{L::BN, L::NQ * BM, &launch_e4m3<128>};
+}
+
+FwdVariant fwd_variant_e4m3_d256() {
+  using L = Layout<256, true>;
+  return FwdVariant{L::BN, L::NQ * BM, &launch_e4m3<256>};
 }
 
 }  // namespace ea51

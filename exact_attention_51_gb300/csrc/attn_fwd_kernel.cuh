@@ -65,14 +65,30 @@ struct Shape<256> {
   static constexpr int BN = 64, NQ = 1, NSB = 2, STAGES = 4;
 };
 
+// e4m3 at d = 256: 128-key tiles (a transposed V tile needs 128-byte rows of
+// keys), one query tile, two S buffers: 2 * 128 + 256 = 512 tensor-memory
+// columns; the 8-bit K/V tiles (32 KiB) fit a four-slot ring.
+struct ShapeE4M3D256 {
+  static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
+};
+template <int D, bool F8>
+struct ShapeOf {
+  using T = Shape<D>;
+};
+template <>
+struct ShapeOf<256, true> {
+  using T = ShapeE4M3D256;
+};
+
 // F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots);
 // the V tile is then stored transposed (D rows of BN keys) so that both MMAs
 // read K-major operands.
 template <int D, bool F8 = false>
 struct Layout {
+  using Sh = typename ShapeOf<D, F8>::T;
   static constexpr int EB = F8 ? 1 : 2;  // bytes per Q/K/V element
-  static constexpr int BN = Shape<D>::BN, NQ = Shape<D>::NQ, NSB = Shape<D>::NSB,
-                       STAGES = F8 ? 2 * Shape<D>::STAGES : Shape<D>::STAGES;
+  static constexpr int BN = Sh::BN, NQ = Sh::NQ, NSB = Sh::NSB,
+                       STAGES = F8 ? 2 * Sh::STAGES : Sh::STAGES;
   static constexpr int PANELS = D * EB / 128;  // 128-byte column panels per Q/K row
   static constexpr int PANEL_ELEMS = 128 / EB;
   static constexpr int KSTEPS_QK = D * EB / 32;   // 32-byte K-steps of S = Q K^T
@@ -120,7 +136,8 @@ struct Layout {
                 "register split exceeds the launch budget");
 
   static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
-  static_assert(!F8 || (D == 128 && BN == 128), "e4m3 tiles: d = 128, 128 keys (one 128-byte row)");
+  static_assert(!F8 || ((D == 128 || D == 256) && BN == 128),
+                "e4m3 tiles: d = 128 or 256, 128 keys (one 128-byte row of V^T)");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1024-byte tile alignment");
@@ -197,9 +214,10 @@ struct Tile {
   int nkv[Shape<D>::NQ];      // key tiles [lo, lo + nkv) visited by each query tile
 };
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) {
-  using L = Layout<D>;
+  using L = Layout<D, F8>;
+  static_assert(L::NQ <= Shape<D>::NQ, "tile bookkeeping sized by the bf16 shape");
   Tile<D, CAUSAL, SPLIT> t;
   const int splits = SPLIT ? p.kv_splits : 1;
   const int cta = blockIdx.x / splits;
@@ -743,7 +761,7 @@ __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT>(p);
+  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8>(p);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
   const Waiter w{abort_flag, p.status};

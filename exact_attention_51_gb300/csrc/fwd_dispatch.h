@@ -56,5 +56,6 @@ FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();
 FwdVariant fwd_variant_d256();
 FwdVariant fwd_variant_e4m3_d128();
+FwdVariant fwd_variant_e4m3_d256();
 
 }  // namespace ea51

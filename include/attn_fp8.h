@@ -29,7 +29,7 @@ extern "C" {
 #endif
 
 /*
- * e4m3 forward, Nq = Nk = N, d = 128.
+ * e4m3 forward, Nq = Nk = N, d = 128 or 256.
  *
  *   q, k, v     e4m3 codes, one byte per element, [B,H,N,d] contiguous,
  *               16-byte aligned; read only.
@@ -43,7 +43,7 @@ extern "C" {
  *               [B*H, d, round_up(N, 16)].  o, lse and workspace must not
  *               overlap each other or q, k, v.
  * Enqueues two kernels on `stream` (the V transpose, then the fused forward)
- * and returns; status codes as in attn_fwd (d != 128, a non-positive or
+ * and returns; status codes as in attn_fwd (d not 128 or 256, a non-positive or
  * non-finite descale, a missing or short workspace: ATTN_ERR_INVALID_ARG).
  */
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q,
@@ -52,7 +52,7 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float des
                           size_t workspace_bytes, void* stream);
 
 /* Workspace bytes for attn_fwd_fp8: B*H*d*round_up(N, 16), 256-byte padded
- * (0 for invalid sizes or d != 128).  Host-only. */
+ * (0 for invalid sizes or d not 128 or 256).  Host-only. */
 ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
 
 #ifdef __cplusplus

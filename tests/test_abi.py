@@ -222,6 +222,7 @@ def test_fp8_workspace_size(lib):
     assert ea.attn_fwd_fp8_workspace_size(1, 2, 256, 128) == 2 * 128 * 256
     assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 128) == 256 * ((128 * 32 + 255) // 256)
     assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 64) == 0
+    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 256) == 256 * ((256 * 32 + 255) // 256)
     assert ea.attn_fwd_fp8_workspace_size(0, 1, 17, 128) == 0
 
 

@@ -72,11 +72,11 @@ SHAPES = [(1, 2, 128), (1, 1, 1), (2, 1, 7), (1, 1, 129), (1, 2, 300), (2, 2, 25
           (1, 1, 2049)]
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("B,H,N", SHAPES, ids=[f"B{b}H{h}N{n}" for b, h, n in SHAPES])
-def test_fp8_small_shapes(B, H, N, causal):
-    d = 128
-    q8, k8, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=7 * N + (1 if causal else 0))
+def test_fp8_small_shapes(B, H, N, causal, d):
+    q8, k8, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=7 * N + d + (1 if causal else 0))
     scale = 1 / math.sqrt(d)
     o, lse = run_fp8(q8, k8, v8, sc, causal, scale)
     o_ref, lse_ref = orc().attn_e4m3(q8, k8, v8, *sc, causal, scale)
@@ -84,7 +84,8 @@ def test_fp8_small_shapes(B, H, N, causal):
     compare(o, o_ref, lse, lse_ref, vmax, f"{(B, H, N, d)} causal={causal}")
 
 
-@pytest.mark.parametrize("name,causal", [("mid", True), ("mid", False), ("long", True)])
+@pytest.mark.parametrize("name,causal", [("mid", True), ("mid", False), ("long", True),
+                                         ("dsweep256", True)])
 def test_fp8_full_size_sampled_rows(name, causal):
     w = wl.WORKLOADS[name]
     q8, k8, v8, sc = wl.make_inputs_e4m3(w.B, w.H, w.N, w.d, w.dist, w.seed, w.k_outlier_frac)
@@ -97,12 +98,13 @@ def test_fp8_full_size_sampled_rows(name, causal):
     compare(o_s, o_ref, lse_s, lse_ref, vmax, f"{name} causal={causal} rows={len(rows)}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_fp8_zero_keys_exact_weights(causal):
+def test_fp8_zero_keys_exact_weights(causal, d):
     """K = 0: every visible score is 0, so every e4m3 weight is exactly 2^7
     (no rounding): O_i = mean of the visible V rows, LSE_i = ln(#visible), to
     the bf16 bar."""
-    B, H, N, d = 1, 2, 300, 128
+    B, H, N = 1, 2, 300
     q8, _, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=3)
     k8 = torch.zeros_like(q8)
     o, lse = run_fp8(q8, k8, v8, (sc[0], 1.0, sc[2]), causal, 1 / math.sqrt(d))
@@ -118,10 +120,11 @@ def test_fp8_zero_keys_exact_weights(causal):
     assert np.abs(lse - lref).max() <= 1e-3
 
 
-def test_fp8_single_key_returns_v():
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_single_key_returns_v(d):
     """N = 1: the one weight is exactly 2^7, so O = descale_v * V8 (exact in
     bf16: 4 significant bits times a power of two) and LSE = scale * s."""
-    B, H, N, d = 2, 3, 1, 128
+    B, H, N = 2, 3, 1
     q8, k8, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=11)
     scale = 1 / math.sqrt(d)
     o, lse = run_fp8(q8, k8, v8, sc, False, scale)
