@@ -98,6 +98,14 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_fp8.restype = _int
         lib.attn_fwd_fp8_workspace_size.argtypes = [_int, _int, _int, _int]
         lib.attn_fwd_fp8_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_fp8_kvcache.argtypes = [_vp, _vp, _vp, _flt, _flt, _flt, _vp, _vp, _int, _int,
+                                             _int, _int, _int, _flt, _int, _int, _vp,
+                                             ctypes.c_size_t, _vp]
+        lib.attn_fwd_fp8_kvcache.restype = _int
+        lib.attn_fwd_fp8_kvcache_workspace_size.argtypes = [_int] * 6
+        lib.attn_fwd_fp8_kvcache_workspace_size.restype = ctypes.c_size_t
+        lib.attn_fwd_fp8_kvcache_num_splits.argtypes = [_int] * 7
+        lib.attn_fwd_fp8_kvcache_num_splits.restype = _int
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.attn_selftest_wait_timeout.restype = _int
         _lib = lib
@@ -212,6 +220,58 @@ def attn_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
             _stream_handle(stream, q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
+    return out, lse
+
+
+def attn_fwd_fp8_kvcache(q, k, v, descale_q: float, descale_k: float, descale_v: float,
+                         causal: bool = False, scale: float | None = None,
+                         num_splits: int | None = None, out=None, lse=None, workspace=None,
+                         stream=None):
+    """e4m3 forward with q [B,H,Nq,d] and k, v [B,H,Nk,d] (d = 128 or 256):
+    the queries are the last Nq positions (causal diagonal at the
+    bottom-right).  ``num_splits`` None picks one from the shape and the SM
+    count.  Returns ``(o, lse)`` as attn_fwd_fp8."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda \
+                or t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be a CUDA float8_e4m3fn (or uint8) tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, H, Nk, d] with q's B, H and d")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = int(lib.attn_fwd_fp8_kvcache_num_splits(B, H, Nq, Nk, d, int(bool(causal)),
+                                                              sms))
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    elif out.shape != (B, H, Nq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous bf16 [B, H, Nq, d] tensor on q's device")
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    elif lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor on q's device")
+    need = int(lib.attn_fwd_fp8_kvcache_workspace_size(B, H, Nq, Nk, d, num_splits))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        rc = lib.attn_fwd_fp8_kvcache(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
+            float(descale_v), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d, float(scale),
+            int(bool(causal)), int(num_splits), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8_kvcache")
     return out, lse
 
 

@@ -266,11 +266,19 @@ int fwd_general(const void* q, const void* k, const void* v, void* o, float* lse
 }
 
 // Split count with the smallest modelled makespan (see include/attn_fwd.h).
+int split_model_for(const ea51::FwdVariant& var, int B, int H, int Nq, int Nk, int causal,
+                    int num_sms);
+
 int split_model(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1)
     return 1;
   if (causal && Nk < Nq) return 1;
-  const ea51::FwdVariant var = variant_for(d);
+  return split_model_for(variant_for(d), B, H, Nq, Nk, causal, num_sms);
+}
+
+// The model for the tile shape of `var` (query rows per CTA, keys per tile).
+int split_model_for(const ea51::FwdVariant& var, int B, int H, int Nq, int Nk, int causal,
+                    int num_sms) {
   const int64_t BH = static_cast<int64_t>(B) * H;
   const int64_t nq = (static_cast<int64_t>(Nq) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
   const int64_t ctas = BH * nq;
@@ -385,35 +393,53 @@ int attn_fwd_device_status(void* stream, unsigned int* detail) {
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
 
-size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return 0;
-  const size_t n_pad = (static_cast<size_t>(N) + 15) / 16 * 16;
-  return align256(static_cast<size_t>(B) * H * d * n_pad);
+}  // extern "C"
+
+namespace {
+
+ea51::FwdVariant fp8_variant(int d) {
+  return d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
 }
 
-int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
-                 float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
-                 int causal, void* workspace, size_t workspace_bytes, void* stream) {
+// e4m3 workspace: V^T [BH, d, round_up(Nk, 16)] bytes, then (split-KV) the
+// fp32 partial O and LSE; `part_off` receives the partials' offset.
+size_t fp8_ws_bytes(int64_t BH, int Nq, int Nk, int d, int splits, size_t* part_off) {
+  const size_t nk_pad = (static_cast<size_t>(Nk) + 15) / 16 * 16;
+  const size_t vt = align256(static_cast<size_t>(BH) * d * nk_pad);
+  if (part_off) *part_off = vt;
+  return vt + (splits > 1 ? splitkv_bytes(BH, Nq, d, splits, nullptr) : 0);
+}
+
+int fp8_general(const void* q, const void* k, const void* v, float descale_q, float descale_k,
+                float descale_v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
+                float scale, int causal, int splits, void* workspace, size_t workspace_bytes,
+                void* stream) {
   if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256)) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
+  if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
   for (const float ds : {descale_q, descale_k, descale_v})
     if (!std::isfinite(ds) || ds <= 0.f) return ATTN_ERR_INVALID_ARG;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  if (BH > 0x7fffffffLL || BH * ((static_cast<int64_t>(N) + 127) / 128) > 0x7fffffffLL ||
-      N > 0x7fffffff - 16)
+  if (BH > 0x7fffffffLL || BH * ((static_cast<int64_t>(Nq) + 127) / 128) * splits > 0x7fffffffLL ||
+      BH * ((static_cast<int64_t>(Nk) + 127) / 128) > 0x7fffffffLL || Nk > 0x7fffffff - 16)
     return ATTN_ERR_INVALID_ARG;
   const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
   if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4) || !al(workspace, 256))
     return ATTN_ERR_MISALIGNED;
-  const size_t need = attn_fwd_fp8_workspace_size(B, H, N, d);
+  size_t part_off = 0;
+  const size_t need = fp8_ws_bytes(BH, Nq, Nk, d, splits, &part_off);
   if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
-  const size_t in_bytes = static_cast<size_t>(BH) * N * d;  // one byte per e4m3 element
+  // one byte per e4m3 element
+  const size_t q_bytes = static_cast<size_t>(BH) * Nq * d, kv_bytes = static_cast<size_t>(BH) * Nk * d;
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {q_bytes, kv_bytes, kv_bytes};
   const void* outs[3] = {o, lse, workspace};
-  const size_t out_bytes[3] = {in_bytes * 2, static_cast<size_t>(BH) * N * 4, need};
+  const size_t out_bytes[3] = {q_bytes * 2, static_cast<size_t>(BH) * Nq * 4, need};
   for (int i = 0; i < 3; ++i) {
-    for (const void* in : {q, k, v})
-      if (overlaps(outs[i], out_bytes[i], in, in_bytes)) return ATTN_ERR_ALIAS;
+    for (int j = 0; j < 3; ++j)
+      if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return ATTN_ERR_ALIAS;
     for (int j = i + 1; j < 3; ++j)
       if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return ATTN_ERR_ALIAS;
   }
@@ -421,35 +447,81 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
   int rc;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int n_pad = (N + 15) / 16 * 16;
-  cudaError_t e = ea51::launch_transpose_v8(v, workspace, BH, N, d, n_pad, st);
+  const int nk_pad = (Nk + 15) / 16 * 16;
+  cudaError_t e = ea51::launch_transpose_v8(v, workspace, BH, Nk, d, nk_pad, st);
   if (e != cudaSuccess) return fail_cuda(e);
-  const ea51::FwdVariant var = d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
+  const ea51::FwdVariant var = fp8_variant(d);
   alignas(64) CUtensorMap tq, tk, tv;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if ((rc = encode_tiled(&tq, q, u8, 1, BH, N, d, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_tiled(&tk, k, u8, 1, BH, N, d, d, var.kv_rows)) != ATTN_OK) return rc;
-  // V^T [BH, d, n_pad]: rows are the d columns of V, keys innermost
-  if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, N, n_pad, d)) != ATTN_OK) return rc;
+  if ((rc = encode_tiled(&tq, q, u8, 1, BH, Nq, d, d, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_tiled(&tk, k, u8, 1, BH, Nk, d, d, var.kv_rows)) != ATTN_OK) return rc;
+  // V^T [BH, d, nk_pad]: rows are the d columns of V, keys innermost
+  if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, Nk, nk_pad, d)) != ATTN_OK) return rc;
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
   p.status = ds->status;
-  p.Nq = N;
-  p.Nk = N;
-  p.causal_off = 0;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal_off = Nk - Nq;
   p.BH = static_cast<int>(BH);
-  p.n_qblk = (N + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
-  const double kv_head = 2.0 * N * d;
+  p.n_qblk = (Nq + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+  const double kv_head = 2.0 * Nk * d;
   const int64_t g = static_cast<int64_t>((64.0 * 1024 * 1024) / kv_head);
   p.heads_per_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * descale_q * descale_k *
                                     1.4426950408889634);
   p.o_scale = descale_v;
-  p.kv_splits = 1;
+  p.kv_splits = splits;
+  size_t lse_off = 0;
+  if (splits > 1) {
+    splitkv_bytes(BH, Nq, d, splits, &lse_off);
+    p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off + lse_off);
+  }
   e = var.launch(&tq, &tk, &tv, p, causal != 0, st);
   if (e != cudaSuccess) return fail_cuda(e);
+  if (splits > 1) {
+    e = ea51::launch_combine(d, p.o_part, p.lse_part, o, lse, BH * Nq, splits, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return 0;
+  return fp8_ws_bytes(static_cast<int64_t>(B) * H, N, N, d, 1, nullptr);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
+                 float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
+                 int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return fp8_general(q, k, v, descale_q, descale_k, descale_v, o, lse, B, H, N, N, d, scale,
+                     causal, 1, workspace, workspace_bytes, stream);
+}
+
+size_t attn_fwd_fp8_kvcache_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256)) return 0;
+  if (num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return fp8_ws_bytes(static_cast<int64_t>(B) * H, Nq, Nk, d, num_splits, nullptr);
+}
+
+int attn_fwd_fp8_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256) || num_sms < 1) return 1;
+  if (causal && Nk < Nq) return 1;
+  return split_model_for(fp8_variant(d), B, H, Nq, Nk, causal, num_sms);
+}
+
+int attn_fwd_fp8_kvcache(const void* q, const void* k, const void* v, float descale_q,
+                         float descale_k, float descale_v, void* o, float* lse, int B, int H,
+                         int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return fp8_general(q, k, v, descale_q, descale_k, descale_v, o, lse, B, H, Nq, Nk, d, scale,
+                     causal, num_splits, workspace, workspace_bytes, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int N) {

@@ -55,6 +55,38 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float des
  * (0 for invalid sizes or d not 128 or 256).  Host-only. */
 ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
 
+/*
+ * e4m3 forward with separate query and key lengths (a KV cache), optionally
+ * split over several CTAs per query block (split-KV, as attn_fwd_splitkv).
+ *
+ *   q           e4m3 [B,H,Nq,d]; k, v e4m3 [B,H,Nk,d]; o bf16 [B,H,Nq,d];
+ *               lse fp32 [B,H,Nq].
+ *   causal      query i sees keys j <= i + Nk - Nq (the queries are the last
+ *               Nq positions of the sequence; needs Nk >= Nq), as
+ *               attn_fwd_kvcache.
+ *   num_splits  1..64; attn_fwd_fp8_kvcache_num_splits gives the
+ *               split count the library's makespan model picks.
+ *   workspace   attn_fwd_fp8_kvcache_workspace_size(B, H, Nq, Nk, d,
+ *               num_splits) bytes, 256-byte aligned: V^T, then (num_splits >
+ *               1) the fp32 partial O and LSE of every split.
+ * Other arguments, errors and asynchrony as attn_fwd_fp8; with num_splits >
+ * 1 a merge kernel follows the fused kernel on `stream`.
+ */
+ATTN_API int attn_fwd_fp8_kvcache(const void* q, const void* k, const void* v, float descale_q,
+                                  float descale_k, float descale_v, void* o, float* lse, int B,
+                                  int H, int Nq, int Nk, int d, float scale, int causal,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* Workspace bytes for attn_fwd_fp8_kvcache (0 for invalid sizes).  Host-only. */
+ATTN_API size_t attn_fwd_fp8_kvcache_workspace_size(int B, int H, int Nq, int Nk, int d,
+                                                    int num_splits);
+
+/* Split count for attn_fwd_fp8_kvcache from the makespan model of
+ * attn_fwd_splitkv_num_splits, for the e4m3 tile shape.  Host-only. */
+ATTN_API int attn_fwd_fp8_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal,
+                                            int num_sms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -85,6 +85,9 @@ def _bind(lib):
     lib.attn_ref_e4m3.argtypes = [_vp, _vp, _vp, _dbl, _dbl, _dbl, _i64, _i64, _i64, _i64,
                                   _dbl, ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
     lib.attn_ref_e4m3.restype = ctypes.c_int
+    lib.attn_ref_e4m3_qk.argtypes = [_vp, _vp, _vp, _dbl, _dbl, _dbl, _i64, _i64, _i64, _i64,
+                                     _i64, _dbl, ctypes.c_int, _vp, _i64, _vp, _vp, ctypes.c_int]
+    lib.attn_ref_e4m3_qk.restype = ctypes.c_int
     lib.attn_ref_e4m3_decode.argtypes = [ctypes.c_int]
     lib.attn_ref_e4m3_decode.restype = _dbl
     lib.attn_ref_max_threads.argtypes = []
@@ -287,6 +290,31 @@ class Oracle:
                                     o.ctypes.data, lse.ctypes.data, int(nthreads))
         if rc:
             raise RuntimeError(f"oracle attn_ref_e4m3 failed: {rc}")
+        return (o, lse) if rows is None else (o[:R], lse[:R])
+
+
+    def attn_e4m3_qk(self, q, k, v, descale_q: float, descale_k: float, descale_v: float,
+                     causal: bool, scale: float, rows=None, nthreads: int = 0):
+        """e4m3 codes, q [B,H,Nq,d] and k, v [B,H,Nk,d] -> (o fp64, lse fp64),
+        whole tensors or the listed flat rows ((b*H+h)*Nq + i)."""
+        qc, kc, vc = (_as_u8(t) for t in (q, k, v))
+        B, H, Nq, Nk, d = _qk_shapes(qc, kc, vc)
+        if rows is None:
+            o = np.empty((B, H, Nq, d), np.float64)
+            lse = np.empty((B, H, Nq), np.float64)
+            rp, R = None, 0
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            R = rows.shape[0]
+            o = np.empty((max(R, 1), d), np.float64)
+            lse = np.empty((max(R, 1),), np.float64)
+            rp = rows.ctypes.data
+        rc = self.lib.attn_ref_e4m3_qk(qc.ctypes.data, kc.ctypes.data, vc.ctypes.data,
+                                       float(descale_q), float(descale_k), float(descale_v),
+                                       B, H, Nq, Nk, d, float(scale), int(bool(causal)), rp, R,
+                                       o.ctypes.data, lse.ctypes.data, int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle attn_ref_e4m3_qk failed: {rc}")
         return (o, lse) if rows is None else (o[:R], lse[:R])
 
 

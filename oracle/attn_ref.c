@@ -296,27 +296,29 @@ static void decode_head_e4m3(const uint8_t *src, double descale, double *dst, in
 double attn_ref_e4m3_decode(int code) { return e4m3_to_f64((uint8_t)(code & 0xff)); }
 
 /*
- * e4m3 inputs with per-tensor dequantisation scales, Nq = Nk = N: attention
- * of (sq * Q8, sk * K8, sv * V8) by the same definition.  rows == NULL: every
- * row, o [B,H,N,d] and lse [B,H,N]; else the nrows flat row ids (b*H + h)*N + i
- * in rows[], results packed in o[r*d..] / lse[r] in that order.
+ * e4m3 inputs with per-tensor dequantisation scales: attention of
+ * (sq * Q8, sk * K8, sv * V8) by the same definition, q [B,H,Nq,d] and k, v
+ * [B,H,Nk,d] (causal needs Nk >= Nq, diagonal at the bottom-right as for bf16
+ * inputs).  rows == NULL: every row, o [B,H,Nq,d] and lse [B,H,Nq]; else the
+ * nrows flat row ids (b*H + h)*Nq + i in rows[], results packed in o[r*d..] /
+ * lse[r] in that order.
  */
-int attn_ref_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, double sq,
-                  double sk, double sv, int64_t B, int64_t H, int64_t N, int64_t d,
-                  double scale, int causal, const int64_t *rows, int64_t nrows,
-                  double *o, double *lse, int nthreads) {
+int attn_ref_e4m3_qk(const uint8_t *q, const uint8_t *k, const uint8_t *v, double sq,
+                     double sk, double sv, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                     int64_t d, double scale, int causal, const int64_t *rows, int64_t nrows,
+                     double *o, double *lse, int nthreads) {
     if (!q || !k || !v || !o || !lse || (rows && nrows < 0)) return ORACLE_EINVAL;
-    int rc = check_sizes(B, H, N, N, d, causal);
+    int rc = check_sizes(B, H, Nq, Nk, d, causal);
     if (rc) return rc;
     if (rows)
         for (int64_t r = 0; r < nrows; ++r)
-            if (rows[r] < 0 || rows[r] >= B * H * N) return ORACLE_EINVAL;
+            if (rows[r] < 0 || rows[r] >= B * H * Nq) return ORACLE_EINVAL;
     set_threads(nthreads);
-    const size_t elems = (size_t)N * (size_t)d;
+    const size_t q_elems = (size_t)Nq * (size_t)d, kv_elems = (size_t)Nk * (size_t)d;
     const int64_t cap = rows ? (nrows ? nrows : 1) : 1;
-    double *Qh = (double *)malloc(elems * sizeof(double));
-    double *Kh = (double *)malloc(elems * sizeof(double));
-    double *Vh = (double *)malloc(elems * sizeof(double));
+    double *Qh = (double *)malloc(q_elems * sizeof(double));
+    double *Kh = (double *)malloc(kv_elems * sizeof(double));
+    double *Vh = (double *)malloc(kv_elems * sizeof(double));
     int64_t *sel = (int64_t *)malloc((size_t)cap * sizeof(int64_t));
     int64_t *pos = (int64_t *)malloc((size_t)cap * sizeof(int64_t));
     double *o_tmp = (double *)malloc((size_t)cap * (size_t)d * sizeof(double));
@@ -329,22 +331,22 @@ int attn_ref_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, double s
         int64_t cnt = 0;
         if (rows) {
             for (int64_t r = 0; r < nrows; ++r)
-                if (rows[r] / N == bh) {
-                    sel[cnt] = rows[r] % N;
+                if (rows[r] / Nq == bh) {
+                    sel[cnt] = rows[r] % Nq;
                     pos[cnt] = r;
                     ++cnt;
                 }
             if (cnt == 0) continue;
         }
-        decode_head_e4m3(q + bh * (int64_t)elems, sq, Qh, (int64_t)elems);
-        decode_head_e4m3(k + bh * (int64_t)elems, sk, Kh, (int64_t)elems);
-        decode_head_e4m3(v + bh * (int64_t)elems, sv, Vh, (int64_t)elems);
+        decode_head_e4m3(q + bh * (int64_t)q_elems, sq, Qh, (int64_t)q_elems);
+        decode_head_e4m3(k + bh * (int64_t)kv_elems, sk, Kh, (int64_t)kv_elems);
+        decode_head_e4m3(v + bh * (int64_t)kv_elems, sv, Vh, (int64_t)kv_elems);
         if (!rows) {
-            rc = head_rows(Qh, Kh, Vh, N, N, d, scale, causal, NULL, N,
-                           o + bh * (int64_t)elems, lse + bh * N);
+            rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, NULL, Nq,
+                           o + bh * (int64_t)q_elems, lse + bh * Nq);
             continue;
         }
-        rc = head_rows(Qh, Kh, Vh, N, N, d, scale, causal, sel, cnt, o_tmp, l_tmp);
+        rc = head_rows(Qh, Kh, Vh, Nq, Nk, d, scale, causal, sel, cnt, o_tmp, l_tmp);
         for (int64_t t = 0; t < cnt && rc == ORACLE_OK; ++t) {
             memcpy(o + pos[t] * d, o_tmp + t * d, (size_t)d * sizeof(double));
             lse[pos[t]] = l_tmp[t];
@@ -353,6 +355,15 @@ int attn_ref_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, double s
 done:
     free(Qh); free(Kh); free(Vh); free(sel); free(pos); free(o_tmp); free(l_tmp);
     return rc;
+}
+
+/* e4m3 inputs, Nq = Nk = N. */
+int attn_ref_e4m3(const uint8_t *q, const uint8_t *k, const uint8_t *v, double sq,
+                  double sk, double sv, int64_t B, int64_t H, int64_t N, int64_t d,
+                  double scale, int causal, const int64_t *rows, int64_t nrows,
+                  double *o, double *lse, int nthreads) {
+    return attn_ref_e4m3_qk(q, k, v, sq, sk, sv, B, H, N, N, d, scale, causal, rows, nrows, o,
+                            lse, nthreads);
 }
 
 /* Threads OpenMP will use for a parallel region (1 without OpenMP). */

@@ -448,12 +448,37 @@ def pin_e4m3_attention(orc):
     return fails
 
 
+def pin_e4m3_rectangular(orc):
+    """e4m3 attention with Nq != Nk equals the fp64 rectangular attention of
+    the dequantised tensors (torch's decoder), whole and by rows."""
+    g = torch.Generator().manual_seed(9)
+    codes = []
+    for shp in ((2, 2, 11, 16), (2, 2, 29, 16), (2, 2, 29, 16)):
+        c = torch.randint(0, 256, shp, generator=g, dtype=torch.int64).to(torch.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x3A
+        codes.append(c)
+    q8, k8, v8 = codes
+    sc = (0.25, 0.5, 2.0)
+    deq = [c.view(torch.float8_e4m3fn).double().numpy() * s for c, s in zip(codes, sc)]
+    fails = []
+    rows = [0, 10, 11, 43, 25]
+    for causal in (False, True):
+        o, lse = orc.attn_e4m3_qk(q8, k8, v8, *sc, causal, 0.03)
+        o2, lse2 = orc.attn_f64_qk(*deq, causal, 0.03)
+        fails += _close(f"e4m3 rect o causal={causal}", o, o2, 0.0)
+        fails += _close(f"e4m3 rect lse causal={causal}", lse, lse2, 0.0)
+        orow, lrow = orc.attn_e4m3_qk(q8, k8, v8, *sc, causal, 0.03, rows=rows)
+        fails += _close(f"e4m3 rect rows o causal={causal}", orow, o.reshape(-1, 16)[rows], 0.0)
+        fails += _close(f"e4m3 rect rows lse causal={causal}", lrow, lse.reshape(-1)[rows], 0.0)
+    return fails
+
+
 ALL_PINS = [
     pin_online_softmax_tiling, pin_merge_law, pin_identity_values, pin_constant_values,
     pin_single_key, pin_uniform_queries, pin_zero_scale, pin_permutation,
     pin_causal_future_blind, pin_key_shift, pin_linearity_in_v, pin_library_sdpa,
     pin_golden, pin_bf16_decode, pin_rows_api, pin_bottom_right_suffix, pin_rectangular_sdpa,
-    pin_rectangular_bf16_rows, pin_e4m3_decode, pin_e4m3_attention,
+    pin_rectangular_bf16_rows, pin_e4m3_decode, pin_e4m3_attention, pin_e4m3_rectangular,
 ]
 
 

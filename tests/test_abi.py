@@ -272,3 +272,30 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call(grads=(dq, dq + n // 2, dv)) == ea.ATTN_ERR_ALIAS  # dk over dq
     assert call(grads=(q, dk, dv)) == ea.ATTN_ERR_ALIAS  # dq over q
     assert ea.attn_bwd_workspace_size(1, 2, 1) == 2 * 256 * ((2 * 128 * 4 + 255) // 256)
+
+
+def test_fp8_kvcache_rejects_bad_arguments(lib):
+    # every call below is invalid, so nothing is ever launched
+    q, k, v, o, lse = ptrs(1 << 24)
+    ws = A + (1 << 30)
+
+    def call(Nq=16, Nk=4096, d=128, causal=1, splits=1, w=ws, wb=None):
+        need = ea.load_library().attn_fwd_fp8_kvcache_workspace_size(1, 2, Nq, Nk, d, splits)
+        return lib.attn_fwd_fp8_kvcache(q, k, v, 1.0, 1.0, 1.0, o, lse, 1, 2, Nq, Nk, d, 0.088,
+                                        causal, splits, w, need if wb is None else wb, None)
+
+    assert call(Nq=4097) == ea.ATTN_ERR_INVALID_ARG          # causal needs Nk >= Nq
+    assert call(d=64) == ea.ATTN_ERR_INVALID_ARG
+    assert call(splits=0) == ea.ATTN_ERR_INVALID_ARG
+    assert call(splits=65) == ea.ATTN_ERR_INVALID_ARG
+    assert call(splits=4, wb=1024) == ea.ATTN_ERR_INVALID_ARG  # workspace too small
+    assert call(w=ws + 16) == ea.ATTN_ERR_MISALIGNED
+    assert call(w=None) == ea.ATTN_ERR_INVALID_ARG
+    # o over the (longer) key tensor: keys span 1*2*4096*128 one-byte codes
+    assert lib.attn_fwd_fp8_kvcache(q, k, v, 1.0, 1.0, 1.0, k + 4096, lse, 1, 2, 16, 4096, 128,
+                                    0.088, 1, 1, ws, 1 << 24, None) == ea.ATTN_ERR_ALIAS
+    f = ea.load_library().attn_fwd_fp8_kvcache_workspace_size
+    assert f(1, 2, 16, 4096, 128, 1) == ea.attn_fwd_fp8_workspace_size(1, 2, 4096, 128)
+    assert f(1, 2, 16, 4096, 128, 4) > f(1, 2, 16, 4096, 128, 1)
+    assert f(1, 2, 16, 4096, 64, 1) == 0
+    assert ea.load_library().attn_fwd_fp8_kvcache_num_splits(1, 8, 1, 32768, 128, 1, 152) >= 2

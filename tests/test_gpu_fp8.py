@@ -132,3 +132,28 @@ def test_fp8_single_key_returns_v(d):
     assert np.array_equal(o, vd)
     s = (q8.view(torch.float8_e4m3fn).double() * k8.view(torch.float8_e4m3fn).double()).sum(-1)
     assert np.abs(lse - (s.numpy() * sc[0] * sc[1] * scale)).max() <= 1e-3
+
+
+KV_SHAPES = [(1, 2, 1, 1000, 128), (1, 2, 7, 4096, 128), (2, 1, 128, 129, 256),
+             (1, 2, 300, 300, 128), (1, 1, 513, 2000, 256), (2, 2, 16, 16384, 128)]
+
+
+@pytest.mark.parametrize("splits", [1, None], ids=["whole", "auto-split"])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,Nq,Nk,d", KV_SHAPES,
+                         ids=[f"B{b}H{h}q{nq}k{nk}d{d}" for b, h, nq, nk, d in KV_SHAPES])
+def test_fp8_kvcache(B, H, Nq, Nk, d, causal, splits):
+    """Queries as the last Nq positions of Nk (bottom-right causal diagonal),
+    whole and split-KV, against the oracle on the dequantised codes."""
+    q = wl.make_inputs(B, H, Nq, d, "normal", seed=Nq + d)[0]
+    _, k, v = wl.make_inputs(B, H, Nk, d, "normal", seed=Nk + d + 1)
+    (q8, sq), (k8, sk), (v8, sv) = (wl.quantize_e4m3(t.float()) for t in (q, k, v))
+    scale = 1 / math.sqrt(d)
+    o, lse = ea.attn_fwd_fp8_kvcache(q8.cuda(), k8.cuda(), v8.cuda(), sq, sk, sv, causal=causal,
+                                     scale=scale, num_splits=splits)
+    st, detail = ea.attn_fwd_device_status()
+    assert st == ea.ATTN_OK, f"device-side wait timed out (code {detail:#x})"
+    o_ref, lse_ref = orc().attn_e4m3_qk(q8, k8, v8, sq, sk, sv, causal, scale)
+    vmax = float(v8.view(torch.float8_e4m3fn).double().abs().max()) * sv
+    compare(o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref, vmax,
+            f"kvcache {(B, H, Nq, Nk, d)} causal={causal} splits={splits}")
