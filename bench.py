@@ -197,6 +197,22 @@ def row_flops(w: wl.Workload, causal: bool, rows) -> float:
     return float(sum(4.0 * w.d * ((r % w.N) + 1) for r in rows))
 
 
+def time_oracle_tiny_one_thread(reps: int = 20):
+    """Median wall time (us) of the oracle on one thread over the whole tiny
+    workload (B=1 H=2 N=128 d=64, non-causal), and its TFLOP/s."""
+    import oracle
+    orc = oracle.Oracle()
+    w = wl.WORKLOADS["tiny"]
+    q, k, v = wl.workload_inputs(w)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        orc.attn_bf16(q, k, v, False, w.scale, nthreads=1)
+        times.append(time.perf_counter() - t0)
+    t = statistics.median(times)
+    return t * 1e6, w.flops(False) / t / 1e12
+
+
 def time_oracle(w, causal, q, k, v, target_s: float, seed: int):
     """Oracle throughput (TFLOP/s) on seeded random row samples, grown until
     one sample takes about `target_s` seconds; returns (tflops, seconds, rows,
@@ -576,6 +592,10 @@ def run_ours(args, w, causal):
                 "value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                 "sample": f"{nrows} seeded random rows of {w.describe(causal)} "
                           f"({secs:.1f} s of fp64 oracle work)"}
+            us1, tf1 = time_oracle_tiny_one_thread()
+            line["cpu_baseline"]["tiny_one_thread"] = {
+                "us": us1, "value": tf1, "unit": "TFLOP/s", "cores": 1,
+                "sample": "the whole tiny workload, B=1 H=2 N=128 d=64 non-causal, median of 20"}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
