@@ -7,7 +7,7 @@
 //   dQ = scale * dS K,  dK = scale * dS^T Q
 //
 // Three kernels, none of them writing an N x N matrix to HBM:
-//   preprocess  D and LSE * log2(e) per row into a padded workspace;
+//   preprocess  -D and -LSE * log2(e) per row into a padded workspace;
 //   dK/dV       one CTA per 128-key block: for every query block it
 //               recomputes S^T = K Q^T and dP^T = V dO^T in tensor memory,
 //               two threads per key row (one per half of the query block)
@@ -105,6 +105,85 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+
+// Four consecutive fp32 values from shared memory (16-byte aligned address).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 r;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "r"(addr));
+  return r;
+}
+
+// P^T and dS^T for one 32-query chunk of one key row (dK/dV kernel):
+//   p = exp2(s * c - lse2_q),  ds = p * (dp - D_q),
+// with nl2 = -lse2 and nds = -D for the chunk's queries at shared-memory
+// address `row` (nds 512 bytes further).  MASKED keeps queries q with
+// lo <= q - col0_block < lo + span only (causal diagonal / ragged tail).
+template <bool MASKED>
+__device__ __forceinline__ void pds_chunk_t(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                            uint32_t row, float c, int col0, int lo, int span,
+                                            uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+  const f32x2 cc = f2_pack(c, c);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 nl = lds_f4(row + 16 * g);
+    const float4 nd = lds_f4(row + 512 + 16 * g);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = 2 * g + u;
+      const f32x2 x = f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), cc,
+                             u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+      float x0, x1;
+      f2_unpack(x, x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if (MASKED) {
+        p0 = static_cast<unsigned>(col0 + 2 * e - lo) < static_cast<unsigned>(span) ? p0 : 0.f;
+        p1 = static_cast<unsigned>(col0 + 2 * e + 1 - lo) < static_cast<unsigned>(span) ? p1 : 0.f;
+      }
+      const f32x2 dd = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                              u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
+      const f32x2 ds = f2_mul(f2_pack(p0, p1), dd);
+      float d0, d1;
+      f2_unpack(ds, d0, d1);
+      pk[e] = pack_bf16x2(p0, p1);
+      dk[e] = pack_bf16x2(d0, d1);
+    }
+  }
+}
+
+// dS for one 32-key chunk of one query row (dQ kernel), with the row's
+// nl2 = -lse2 and nds = -D; MASKED keeps keys col0 + i < lim only.
+template <bool MASKED>
+__device__ __forceinline__ void ds_chunk_q(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                           float c, float nl2, float nds, int col0, int lim,
+                                           uint32_t (&dk)[16]) {
+  const f32x2 cc = f2_pack(c, c), nl = f2_pack(nl2, nl2), nd = f2_pack(nds, nds);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const f32x2 x =
+        f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), cc, nl);
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (MASKED) {
+      p0 = col0 + 2 * e < lim ? p0 : 0.f;
+      p1 = col0 + 2 * e + 1 < lim ? p1 : 0.f;
+    }
+    const f32x2 ds = f2_mul(
+        f2_pack(p0, p1),
+        f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), nd));
+    float d0, d1;
+    f2_unpack(ds, d0, d1);
+    dk[e] = pack_bf16x2(d0, d1);
+  }
+}
+
 // ------------------------------------------------------------ preprocess
 
 __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
@@ -127,13 +206,13 @@ __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
       const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + row * d + c);
       acc += __bfloat162float(a.x) * __bfloat162float(g.x) + __bfloat162float(a.y) * __bfloat162float(g.y);
     }
-    l2 = lse[row] * 1.4426950408889634f;
+    l2 = -lse[row] * 1.4426950408889634f;
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    lse2[bh * Npad + i] = l2;
-    dsum[bh * Npad + i] = acc;
+    lse2[bh * Npad + i] = l2;    // -LSE * log2(e)
+    dsum[bh * Npad + i] = -acc;  // -D
   }
 }
 
@@ -317,10 +396,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
       if (!ok) break;
       tc_fence_after_sync();
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::A_OFF_RING + st * L::A_STAGE + 2 * L::TILE);
-      const float* dsm = lse2 + 128;
-      const bool diag = CAUSAL && qblk == kb;     // key > query masked inside
+      // -lse2 and -D of the block's queries (shared memory, written by the TMA)
+      const uint32_t rowv = sbase + L::A_OFF_RING + st * L::A_STAGE + 2 * L::TILE;
+      const bool diag = CAUSAL && qblk == kb;     // queries < key masked
       const bool tail = qblk * 128 + 128 > p.N;  // queries >= N masked
+      // visible queries of this key row: [lo, lo + span) within the block
+      const int lo = diag ? r : 0;
+      const int span = max(0, (tail ? p.N - qblk * 128 : 128) - lo);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         // chunk c2 of this half, then its packed result at packed_col(h) + 16 c2
@@ -330,20 +412,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait(s);
         tmem_ld_wait(dp);
         uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = h * 64 + c2 * 32 + 2 * e + u;  // query within the block
-            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + u]), c, -lse2[col]));
-            if ((diag && key > qblk * 128 + col) || (tail && qblk * 128 + col >= p.N)) pp = 0.f;
-            pv[u] = pp;
-            dv[u] = pp * (__uint_as_float(dp[2 * e + u]) - dsm[col]);
-          }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk[e] = pack_bf16x2(dv[0], dv[1]);
-        }
+        const int col0 = h * 64 + c2 * 32;  // first query of the chunk within the block
+        if (diag || tail)
+          pds_chunk_t<true>(s, dp, rowv + 4 * col0, c, col0, lo, span, pk, dk);
+        else
+          pds_chunk_t<false>(s, dp, rowv + 4 * col0, c, col0, lo, span, pk, dk);
         tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, pk);
         tmem_st_32x32b_x16(tmem + lb + L::T2 + packed_col(h) + c2 * 16, dk);
       }
@@ -548,8 +621,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lb = static_cast<uint32_t>(qd * 32) << 16;
     const float c = p.scale_log2;
     const size_t prow = static_cast<size_t>(bh) * p.Npad + qrow;
-    const float l2 = p.lse2[prow];
-    const float dsum = p.dsum[prow];
+    const float nl2 = p.lse2[prow];   // -LSE * log2(e)
+    const float nds = p.dsum[prow];   // -D
     bool ok = true;
     for (int t = 0; t < nk && ok; ++t) {
       ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
@@ -568,18 +641,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_wait(s);
         tmem_ld_wait(dp);
         uint32_t dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = h * 64 + c2 * 32 + 2 * e + u;  // key within the block
-            float pp = ex2_approx(fmaf(__uint_as_float(s[2 * e + u]), c, -l2));
-            if ((diag || tail) && col >= lim) pp = 0.f;
-            dv[u] = pp * (__uint_as_float(dp[2 * e + u]) - dsum);
-          }
-          dk[e] = pack_bf16x2(dv[0], dv[1]);
-        }
+        const int col0 = h * 64 + c2 * 32;  // first key of the chunk within the block
+        if (diag || tail)
+          ds_chunk_q<true>(s, dp, c, nl2, nds, col0, lim, dk);
+        else
+          ds_chunk_q<false>(s, dp, c, nl2, nds, col0, lim, dk);
         tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, dk);
       }
       tmem_st_wait();

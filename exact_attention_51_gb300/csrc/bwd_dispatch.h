@@ -10,8 +10,8 @@ struct BwdParams {
   __nv_bfloat16* dq;     // bf16 [BH, N, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* lse2;           // workspace: LSE * log2(e), [BH, Npad]
-  float* dsum;           // workspace: D = rowsum(dO o O), [BH, Npad]
+  float* lse2;           // workspace: -LSE * log2(e), [BH, Npad]
+  float* dsum;           // workspace: -D, D = rowsum(dO o O), [BH, Npad]
   unsigned int* status;  // device-wide wait-timeout word
   int N;
   int Npad;              // N rounded up to 128
