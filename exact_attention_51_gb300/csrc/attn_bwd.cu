@@ -11,12 +11,15 @@
 //   dK/dV       one CTA per 128-key block: for every query block it
 //               recomputes S^T = K Q^T and dP^T = V dO^T in tensor memory,
 //               two threads per key row (one per half of the query block)
-//               form P^T and dS^T (bf16, written over the fp32 tiles), and
-//               the tensor core accumulates
-//               dV += P^T dO and dK += dS^T Q in tensor memory;
+//               form P^T, then dS^T (bf16, written over the fp32 tiles; P
+//               stays in fp32 registers in between), and the tensor core
+//               accumulates dV += P^T dO and dK += dS^T Q in tensor memory;
 //   dQ          one CTA per 128-query block: recomputes S and dP per key
-//               block, forms dS (two threads per query row), accumulates
-//               dQ += dS K.
+//               block, forms P then dS (two threads per query row),
+//               accumulates dQ += dS K.
+// In both, the MMA of the next block's S runs as soon as the elementwise
+// warps are done with the current one, so their exponentials overlap the
+// tensor core's other products.
 // S and dP are computed twice (once per kernel) so that no kernel needs a
 // transposed copy of dS or atomics: every MMA uses the operand layouts of the
 // forward kernel (K-major A/B from shared memory, or A from tensor memory
@@ -35,8 +38,7 @@
 namespace ea51 {
 namespace {
 
-constexpr int BQ = 128;  // query rows per tile
-constexpr int BK = 128;  // key rows per tile
+// Tiles of 128 query rows by 128 key rows throughout.
 // Warps: 0..7 elementwise (two per tensor-memory lane quadrant, each taking
 // half of the tile's 128 columns), 8 TMA, 9 MMA.
 constexpr int kComputeWarps = 8;
@@ -64,8 +66,9 @@ struct BwdLayout {
   static constexpr int B_STAGE = 2 * TILE;
   static constexpr int B_OFF_BAR = B_OFF_RING + STAGES * B_STAGE;
   // barriers (both kernels): 0 resident-full, [1, 1+ST) ring full,
-  // [1+ST, 1+2ST) ring empty, s_full[2 column halves], p_ready[2 halves],
-  // final, drain
+  // [1+ST, 1+2ST) ring empty, BAR_S: S (or S^T) computed, BAR_S + 1: dP (or
+  // dP^T) computed; BAR_P: P^T packed (dK/dV) or S read out (dQ), BAR_P + 1:
+  // dS (or dS^T) packed, each counted once per elementwise warp; final, drain
   static constexpr int BAR_RES = 0, BAR_FULL = 1, BAR_EMPTY = 1 + STAGES, BAR_S = 1 + 2 * STAGES,
                        BAR_P = BAR_S + 2, BAR_FINAL = BAR_P + 2, BAR_DRAIN = BAR_FINAL + 1,
                        NBAR = BAR_DRAIN + 1;
@@ -120,25 +123,23 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   return r;
 }
 
-// P^T and dS^T for one 32-query chunk of one key row (dK/dV kernel):
-//   p = exp2(s * c - lse2_q),  ds = p * (dp - D_q),
-// with nl2 = -lse2 and nds = -D for the chunk's queries at shared-memory
-// address `row` (nds 512 bytes further).  MASKED keeps queries q with
-// lo <= q - col0_block < lo + span only (causal diagonal / ragged tail).
+// p = exp2(s * c - lse2_q) for one 32-query chunk of one key row (dK/dV
+// kernel), in place over the chunk's S^T bits, with the chunk's -lse2 at
+// shared-memory address `row`; also packs P^T to bf16.  MASKED keeps queries
+// q with lo <= q < lo + span (block-relative) only (causal diagonal, ragged
+// tail).
 template <bool MASKED>
-__device__ __forceinline__ void pds_chunk_t(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                            uint32_t row, float c, int col0, int lo, int span,
-                                            uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+__device__ __forceinline__ void p_chunk_t(uint32_t (&sp)[32], uint32_t row, float c, int col0,
+                                          int lo, int span, uint32_t (&pk)[16]) {
   const f32x2 cc = f2_pack(c, c);
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     const float4 nl = lds_f4(row + 16 * g);
-    const float4 nd = lds_f4(row + 512 + 16 * g);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int e = 2 * g + u;
-      const f32x2 x = f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), cc,
-                             u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+      const f32x2 x = f2_fma(f2_pack(__uint_as_float(sp[2 * e]), __uint_as_float(sp[2 * e + 1])),
+                             cc, u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
       float x0, x1;
       f2_unpack(x, x0, x1);
       float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -146,28 +147,23 @@ __device__ __forceinline__ void pds_chunk_t(const uint32_t (&s)[32], const uint3
         p0 = static_cast<unsigned>(col0 + 2 * e - lo) < static_cast<unsigned>(span) ? p0 : 0.f;
         p1 = static_cast<unsigned>(col0 + 2 * e + 1 - lo) < static_cast<unsigned>(span) ? p1 : 0.f;
       }
-      const f32x2 dd = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                              u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
-      const f32x2 ds = f2_mul(f2_pack(p0, p1), dd);
-      float d0, d1;
-      f2_unpack(ds, d0, d1);
+      sp[2 * e] = __float_as_uint(p0);
+      sp[2 * e + 1] = __float_as_uint(p1);
       pk[e] = pack_bf16x2(p0, p1);
-      dk[e] = pack_bf16x2(d0, d1);
     }
   }
 }
 
-// dS for one 32-key chunk of one query row (dQ kernel), with the row's
-// nl2 = -lse2 and nds = -D; MASKED keeps keys col0 + i < lim only.
+// p = exp2(s * c - lse2) for one 32-key chunk of one query row (dQ kernel),
+// in place, with the row's nl2 = -lse2; MASKED keeps keys col0 + i < lim.
 template <bool MASKED>
-__device__ __forceinline__ void ds_chunk_q(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                           float c, float nl2, float nds, int col0, int lim,
-                                           uint32_t (&dk)[16]) {
-  const f32x2 cc = f2_pack(c, c), nl = f2_pack(nl2, nl2), nd = f2_pack(nds, nds);
+__device__ __forceinline__ void p_chunk_q(uint32_t (&sp)[32], float c, float nl2, int col0,
+                                          int lim) {
+  const f32x2 cc = f2_pack(c, c), nl = f2_pack(nl2, nl2);
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const f32x2 x =
-        f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), cc, nl);
+        f2_fma(f2_pack(__uint_as_float(sp[2 * e]), __uint_as_float(sp[2 * e + 1])), cc, nl);
     float x0, x1;
     f2_unpack(x, x0, x1);
     float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
@@ -175,15 +171,45 @@ __device__ __forceinline__ void ds_chunk_q(const uint32_t (&s)[32], const uint32
       p0 = col0 + 2 * e < lim ? p0 : 0.f;
       p1 = col0 + 2 * e + 1 < lim ? p1 : 0.f;
     }
+    sp[2 * e] = __float_as_uint(p0);
+    sp[2 * e + 1] = __float_as_uint(p1);
+  }
+}
+
+// ds = p * (dp - D) for one 32-column chunk, packed to bf16, with -D per
+// column (dK/dV kernel: four at a time from shared memory at `nd_row`).
+__device__ __forceinline__ void ds_chunk_t(const uint32_t (&p)[32], const uint32_t (&dp)[32],
+                                           uint32_t nd_row, uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float4 nd = lds_f4(nd_row + 16 * g);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = 2 * g + u;
+      const f32x2 dd = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                              u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y));
+      const f32x2 ds = f2_mul(f2_pack(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])), dd);
+      float d0, d1;
+      f2_unpack(ds, d0, d1);
+      dk[e] = pack_bf16x2(d0, d1);
+    }
+  }
+}
+
+// The same with one -D for the whole chunk (dQ kernel: one query row).
+__device__ __forceinline__ void ds_chunk_q(const uint32_t (&p)[32], const uint32_t (&dp)[32],
+                                           float nds, uint32_t (&dk)[16]) {
+  const f32x2 nd = f2_pack(nds, nds);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
     const f32x2 ds = f2_mul(
-        f2_pack(p0, p1),
+        f2_pack(__uint_as_float(p[2 * e]), __uint_as_float(p[2 * e + 1])),
         f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), nd));
     float d0, d1;
     f2_unpack(ds, d0, d1);
     dk[e] = pack_bf16x2(d0, d1);
   }
 }
-
 // ------------------------------------------------------------ preprocess
 
 __global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
@@ -250,7 +276,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i)
-      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps / 2 : 1u);
+      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -301,12 +327,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     const uint32_t leader = elect_one();
-    // Work is split by query-column half: S^T and dP^T of block t+1 for the
-    // first 64 queries are computed while the elementwise warps of the second
-    // half still work on block t, so the tensor core keeps busy while each
-    // half forms its P^T and dS^T.
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 64, false);  // S^T, dP^T halves: K-major
-    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);    // dV, dK: B MN-major
+    // Order per query block t: dV(t), S^T(t+1), dK(t), dP^T(t+1).  The
+    // exponentials of block t+1 (waiting on S^T(t+1)) run while the tensor
+    // core works on dK(t) and dP^T(t+1); dS^T(t+1) is formed while it runs
+    // dV(t+1) and S^T(t+2).
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);  // S^T, dP^T: K-major
+    constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);      // dV, dK: B MN-major
     bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
     const uint64_t dK0 = sdesc_sw128(sbase + L::A_OFF_K, 16, 1024);
     const uint64_t dV0 = sdesc_sw128(sbase + L::A_OFF_V, 16, 1024);
@@ -317,60 +343,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return warp_wait_phase(bar(L::BAR_FULL + t % L::STAGES),
                              static_cast<uint32_t>(t / L::STAGES) & 1u, w, kCodeMmaKV);
     };
-    // S^T = K Q^T and dP^T = V dO^T of block t for queries [64 hh, 64 hh + 64)
-    auto issue_sdp = [&](int t, int hh) {
-      const uint32_t base = stage_base(t) + hh * 64 * 128;  // 64 rows into each 128-byte panel
-      const uint64_t qK = sdesc_sw128(base, 16, 1024);
-      const uint64_t oK = sdesc_sw128(base + L::TILE, 16, 1024);
+    // S^T = K Q^T of query block t (into T1)
+    auto issue_s = [&](int t) {
+      const uint64_t qK = sdesc_sw128(stage_base(t), 16, 1024);
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T1 + 64 * hh, dK0 + off, qK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
+        mma_ss(tmem + L::T1, dK0 + off, qK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T2 + 64 * hh, dV0 + off, oK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
-      }
-      mma_commit(bar(L::BAR_S + hh), leader);
+      mma_commit(bar(L::BAR_S), leader);
     };
-    // dV += P^T dO and dK += dS^T Q over queries [64 hh, 64 hh + 64) of block t
-    auto issue_acc = [&](int t, int hh) {
-      const uint32_t base = stage_base(t);
-      const uint64_t qM = sdesc_sw128(base, L::PANEL, 1024);            // Q as MN-major B
-      const uint64_t oM = sdesc_sw128(base + L::TILE, L::PANEL, 1024);  // dO as MN-major B
+    // dP^T = V dO^T of query block t (into T2)
+    auto issue_dp = [&](int t) {
+      const uint64_t oK = sdesc_sw128(stage_base(t) + L::TILE, 16, 1024);
 #pragma unroll
-      for (int k = 4 * hh; k < 4 * hh + 4; ++k) {
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T2, dV0 + off, oK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
+      }
+      mma_commit(bar(L::BAR_S + 1), leader);
+    };
+    // acc += A B over the block's 128 queries: A = packed P^T or dS^T in
+    // tensor memory, B = dO or Q (MN-major)
+    auto issue_acc = [&](int t, uint32_t acc_col, uint32_t a_base, uint32_t b_off) {
+      const uint64_t bM = sdesc_sw128(stage_base(t) + b_off, L::PANEL, 1024);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
-        const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-        mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), oM + bo, kIdescTS, acc, leader);  // dV
-        mma_ts(tmem + L::ACC1, tmem + L::T2 + a_col(k), qM + bo, kIdescTS, acc, leader);  // dK
+        mma_ts(tmem + acc_col, tmem + a_base + a_col(k), bM + bo, kIdescTS,
+               (t > 0 || k > 0) ? 1u : 0u, leader);
       }
     };
     if (ok && nq > 0) {
       ok = wait_stage(0);
       if (ok) {
-        issue_sdp(0, 0);
-        issue_sdp(0, 1);
+        issue_s(0);
+        issue_dp(0);
       }
     }
     for (int t = 0; t < nq && ok; ++t) {
       const uint32_t ph = static_cast<uint32_t>(t) & 1u;
-      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);
+      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);  // P^T(t) packed in T1
       if (!ok) break;
       tc_fence_after_sync();
-      issue_acc(t, 0);
+      issue_acc(t, L::ACC0, L::T1, L::TILE);  // dV += P^T dO
       if (t + 1 < nq) {
         ok = wait_stage(t + 1);
         if (!ok) break;
-        issue_sdp(t + 1, 0);  // over the first half's P^T / dS^T, read by the MMAs above
+        issue_s(t + 1);  // over P^T(t), read by the MMAs above
       }
-      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);
+      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);  // dS^T(t) packed in T2
       if (!ok) break;
       tc_fence_after_sync();
-      issue_acc(t, 1);
+      issue_acc(t, L::ACC1, L::T2, 0);  // dK += dS^T Q
       mma_commit(bar(L::BAR_EMPTY + t % L::STAGES), leader);
-      if (t + 1 < nq) issue_sdp(t + 1, 1);
+      if (t + 1 < nq) issue_dp(t + 1);  // over dS^T(t)
     }
     if (ok) mma_commit(bar(L::BAR_FINAL), leader);
     if (!ok) {
@@ -379,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
   } else if (warp < kComputeWarps) {
-    // ---------------------- P^T, dS^T: one key row per thread, half the queries
+    // ------------- P^T, then dS^T: one key row per thread, 64 of the queries
     const int qd = warp & 3, h = warp >> 2;  // lane quadrant, column half
     const int r = qd * 32 + lane;  // key row in the block == TMEM lane
     const int key = kb * 128 + r;
@@ -389,11 +416,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int t = 0; t < nq && ok; ++t) {
       const int st = t % L::STAGES;
       const int qblk = q_first + t;
-      // the stage's LSE / D rows were written by the TMA: wait on its barrier
-      // too before reading them from shared memory
+      const uint32_t ph = static_cast<uint32_t>(t) & 1u;
+      // the stage's -lse2 / -D rows were written by the TMA: wait on its
+      // barrier too before reading them from shared memory
       ok = warp_wait_phase(bar(L::BAR_FULL + st), static_cast<uint32_t>(t / L::STAGES) & 1u, w,
                            kCodeSoftS);
-      if (ok) ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      if (ok) ok = warp_wait_phase(bar(L::BAR_S), ph, w, kCodeSoftS);
       if (!ok) break;
       tc_fence_after_sync();
       // -lse2 and -D of the block's queries (shared memory, written by the TMA)
@@ -403,27 +431,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // visible queries of this key row: [lo, lo + span) within the block
       const int lo = diag ? r : 0;
       const int span = max(0, (tail ? p.N - qblk * 128 : 128) - lo);
+      // S^T of this thread's 64 queries, then P^T in fp32 (kept for dS^T)
+      uint32_t pr[2][32];
+      tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64, pr[0]);
+      tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + 32, pr[1]);
+      tmem_ld_wait(pr[0]);
+      tmem_ld_wait(pr[1]);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        // chunk c2 of this half, then its packed result at packed_col(h) + 16 c2
-        uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + c2 * 32, s);
-        tmem_ld_32x32b_x32(tmem + lb + L::T2 + h * 64 + c2 * 32, dp);
-        tmem_ld_wait(s);
-        tmem_ld_wait(dp);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
         const int col0 = h * 64 + c2 * 32;  // first query of the chunk within the block
         if (diag || tail)
-          pds_chunk_t<true>(s, dp, rowv + 4 * col0, c, col0, lo, span, pk, dk);
+          p_chunk_t<true>(pr[c2], rowv + 4 * col0, c, col0, lo, span, pk);
         else
-          pds_chunk_t<false>(s, dp, rowv + 4 * col0, c, col0, lo, span, pk, dk);
+          p_chunk_t<false>(pr[c2], rowv + 4 * col0, c, col0, lo, span, pk);
         tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::BAR_P));
+      // dS^T = P^T o (dP^T - D)
+      ok = warp_wait_phase(bar(L::BAR_S + 1), ph, w, kCodeSoftS);
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t dp[32], dk[16];
+        const int col0 = h * 64 + c2 * 32;
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + col0, dp);
+        tmem_ld_wait(dp);
+        ds_chunk_t(pr[c2], dp, rowv + 512 + 4 * col0, dk);
         tmem_st_32x32b_x16(tmem + lb + L::T2 + packed_col(h) + c2 * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::BAR_P + h));
+      if (lane == 0) mbar_arrive(bar(L::BAR_P + 1));
     }
     if (ok && nq > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
     if (ok) {
@@ -497,7 +541,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::NBAR; ++i)
-      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps / 2 : 1u);
+      mbar_init(bar(i), (i == L::BAR_P || i == L::BAR_P + 1) ? kComputeWarps : 1u);
     *abort_flag = 0u;
     fence_mbarrier_init();
   }
@@ -542,9 +586,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     const uint32_t leader = elect_one();
-    // Split by key-column half as in the dK/dV kernel: S and dP of block t+1
-    // for the first 64 keys overlap the second half's work on block t.
-    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 64, false);
+    // Order per key block t: S(t+1) as soon as the elementwise warps have
+    // read S(t), then dQ(t), then dP(t+1): the exponentials of block t+1 run
+    // while the tensor core works on dQ(t) and dP(t+1).
+    constexpr uint32_t kIdescSS = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescTS = idesc_bf16_f32(128, D, true);
     bool ok = warp_wait_phase(bar(L::BAR_RES), 0u, w, kCodeMmaQ);
     const uint64_t qA = sdesc_sw128(sbase + L::B_OFF_Q, 16, 1024);
@@ -556,57 +601,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return warp_wait_phase(bar(L::BAR_FULL + t % L::STAGES),
                              static_cast<uint32_t>(t / L::STAGES) & 1u, w, kCodeMmaKV);
     };
-    // S = Q K^T and dP = dO V^T of key block t for keys [64 hh, 64 hh + 64)
-    auto issue_sdp = [&](int t, int hh) {
-      const uint32_t base = stage_base(t) + hh * 64 * 128;
-      const uint64_t kK = sdesc_sw128(base, 16, 1024);
-      const uint64_t vK = sdesc_sw128(base + L::TILE, 16, 1024);
+    // S = Q K^T of key block t (into T1)
+    auto issue_s = [&](int t) {
+      const uint64_t kK = sdesc_sw128(stage_base(t), 16, 1024);
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T1 + 64 * hh, qA + off, kK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
+        mma_ss(tmem + L::T1, qA + off, kK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
       }
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
-        mma_ss(tmem + L::T2 + 64 * hh, oA + off, vK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
-      }
-      mma_commit(bar(L::BAR_S + hh), leader);
+      mma_commit(bar(L::BAR_S), leader);
     };
-    // dQ += dS K over keys [64 hh, 64 hh + 64) of block t
-    auto issue_dq = [&](int t, int hh) {
+    // dP = dO V^T of key block t (into T2)
+    auto issue_dp = [&](int t) {
+      const uint64_t vK = sdesc_sw128(stage_base(t) + L::TILE, 16, 1024);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k / 4) * L::PANEL + (k % 4) * 32) >> 4;
+        mma_ss(tmem + L::T2, oA + off, vK + off, kIdescSS, k > 0 ? 1u : 0u, leader);
+      }
+      mma_commit(bar(L::BAR_S + 1), leader);
+    };
+    // dQ += dS K over the block's 128 keys (dS packed in T2)
+    auto issue_dq = [&](int t) {
       const uint64_t kM = sdesc_sw128(stage_base(t), L::PANEL, 1024);
 #pragma unroll
-      for (int k = 4 * hh; k < 4 * hh + 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const uint32_t bo = (k * 16 * 128) >> 4;
-        mma_ts(tmem + L::ACC0, tmem + L::T1 + a_col(k), kM + bo, kIdescTS,
+        mma_ts(tmem + L::ACC0, tmem + L::T2 + a_col(k), kM + bo, kIdescTS,
                (t > 0 || k > 0) ? 1u : 0u, leader);
       }
     };
     if (ok && nk > 0) {
       ok = wait_stage(0);
       if (ok) {
-        issue_sdp(0, 0);
-        issue_sdp(0, 1);
+        issue_s(0);
+        issue_dp(0);
       }
     }
     for (int t = 0; t < nk && ok; ++t) {
       const uint32_t ph = static_cast<uint32_t>(t) & 1u;
-      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);
+      ok = warp_wait_phase(bar(L::BAR_P), ph, w, kCodeMmaP);  // S(t) read out of T1
       if (!ok) break;
-      tc_fence_after_sync();
-      issue_dq(t, 0);
       if (t + 1 < nk) {
         ok = wait_stage(t + 1);
         if (!ok) break;
-        issue_sdp(t + 1, 0);
+        tc_fence_after_sync();
+        issue_s(t + 1);
       }
-      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);
+      ok = warp_wait_phase(bar(L::BAR_P + 1), ph, w, kCodeMmaP);  // dS(t) packed in T2
       if (!ok) break;
       tc_fence_after_sync();
-      issue_dq(t, 1);
+      issue_dq(t);
       mma_commit(bar(L::BAR_EMPTY + t % L::STAGES), leader);
-      if (t + 1 < nk) issue_sdp(t + 1, 1);
+      if (t + 1 < nk) issue_dp(t + 1);  // over dS(t), read by the MMAs above
     }
     if (ok) mma_commit(bar(L::BAR_FINAL), leader);
     if (!ok) {
@@ -625,9 +672,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float nds = p.dsum[prow];   // -D
     bool ok = true;
     for (int t = 0; t < nk && ok; ++t) {
-      ok = warp_wait_phase(bar(L::BAR_S + h), static_cast<uint32_t>(t) & 1u, w, kCodeSoftS);
+      const uint32_t ph = static_cast<uint32_t>(t) & 1u;
+      ok = warp_wait_phase(bar(L::BAR_S), ph, w, kCodeSoftS);
       if (!ok) break;
       tc_fence_after_sync();
+      // S of this thread's 64 keys; T1 is free for S(t+1) once they are read
+      uint32_t pr[2][32];
+      tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64, pr[0]);
+      tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + 32, pr[1]);
+      tmem_ld_wait(pr[0]);
+      tmem_ld_wait(pr[1]);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::BAR_P));
       const bool diag = CAUSAL && t == qb;
       const bool tail = t * 128 + 128 > p.N;
       int lim = 128;  // keys [0, lim) of this block are visible
@@ -635,23 +692,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (diag) lim = min(lim, qrow - t * 128 + 1);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(tmem + lb + L::T1 + h * 64 + c2 * 32, s);
-        tmem_ld_32x32b_x32(tmem + lb + L::T2 + h * 64 + c2 * 32, dp);
-        tmem_ld_wait(s);
-        tmem_ld_wait(dp);
-        uint32_t dk[16];
         const int col0 = h * 64 + c2 * 32;  // first key of the chunk within the block
         if (diag || tail)
-          ds_chunk_q<true>(s, dp, c, nl2, nds, col0, lim, dk);
+          p_chunk_q<true>(pr[c2], c, nl2, col0, lim);
         else
-          ds_chunk_q<false>(s, dp, c, nl2, nds, col0, lim, dk);
-        tmem_st_32x32b_x16(tmem + lb + L::T1 + packed_col(h) + c2 * 16, dk);
+          p_chunk_q<false>(pr[c2], c, nl2, col0, lim);
+      }
+      // dS = P o (dP - D), packed over the dP columns already read
+      ok = warp_wait_phase(bar(L::BAR_S + 1), ph, w, kCodeSoftS);
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t dp[32], dk[16];
+        const int col0 = h * 64 + c2 * 32;
+        tmem_ld_32x32b_x32(tmem + lb + L::T2 + col0, dp);
+        tmem_ld_wait(dp);
+        ds_chunk_q(pr[c2], dp, nds, dk);
+        tmem_st_32x32b_x16(tmem + lb + L::T2 + packed_col(h) + c2 * 16, dk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::BAR_P + h));
+      if (lane == 0) mbar_arrive(bar(L::BAR_P + 1));
     }
     if (ok && nk > 0) ok = warp_wait_phase(bar(L::BAR_FINAL), 0u, w, kCodeSoftFinal);
     if (ok) {
