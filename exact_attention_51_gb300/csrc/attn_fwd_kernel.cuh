@@ -62,7 +62,9 @@ struct Shape<128> {
 };
 template <>
 struct Shape<256> {
-  static constexpr int BN = 64, NQ = 1, NSB = 2, STAGES = 4;
+  // 2 * 128 + 256 = 512 tensor-memory columns; Q + one K and one V tile =
+  // 192 KiB of shared memory
+  static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
 };
 
 // e4m3 at d = 256: 128-key tiles (a transposed V tile needs 128-byte rows of
@@ -123,6 +125,10 @@ struct Layout {
   // warps: [0, 4*NQ) softmax warpgroups, then TMA, MMA, two spare warps
   static constexpr int TMA_WARP = 4 * NQ;
   static constexpr int MMA_WARP = 4 * NQ + 1;
+  // bf16 d = 256: K and V tiles loaded by two producer warps (V_WARP the V
+  // tiles); the e4m3 shape's four ring slots keep up with one
+  static constexpr bool SPLIT_LOAD = D == 256 && !F8;
+  static constexpr int V_WARP = 4 * NQ + 2;
   static constexpr int THREADS = (NQ + 1) * 128;
   // Register split (setmaxnreg) when the launch budget per thread is tight:
   // 384 threads launch with 168 registers each (65536 / 384, rounded down to
@@ -266,18 +272,26 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
   return t;
 }
 
+// One lane runs this and loads Q, then K_0, V_0, K_1, ... in ring order.
+// With SPLIT_LOAD, lanes of two warps run it: `par` = 0 loads Q and the K
+// tiles (even ring positions), `par` = 1 the V tiles (odd positions); with an
+// even number of ring slots K and V use disjoint slots, so a K tile is never
+// queued behind a V tile whose slot P.V is still reading (with one K and one
+// V slot, the next K loads during P.V and the next V during the next S).
 template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
-                              Waiter w) {
+                              Waiter w, int par) {
   using L = Layout<D, F8>;
+  static_assert(!L::SPLIT_LOAD || L::STAGES % 2 == 0, "K and V take alternate ring slots");
+  constexpr int STEP = L::SPLIT_LOAD ? 2 : 1;
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   int nkv = 0;
 #pragma unroll
   for (int q = 0; q < L::NQ; ++q) {
     nkv = max(nkv, t.nkv[q]);
-    if (t.nkv[q] > 0) {
+    if (t.nkv[q] > 0 && par == 0) {
       const uint32_t fb = bar(L::B_QFULL + q);
       mbar_arrive_expect_tx(fb, L::Q_BYTES);
 #pragma unroll
@@ -287,8 +301,8 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     }
   }
   const int total = 2 * nkv;  // K_0, V_0, K_1, V_1, ...
-  int issued = 0;
-  for (int i = 0; i < total; ++i) {
+  int next = par;  // next ring position of this lane
+  for (int i = par; i < total; i += STEP) {
     const int st = i % L::STAGES;
     const uint32_t ph = static_cast<uint32_t>(i / L::STAGES) & 1u;
     if (!wait_phase(bar(L::B_KVEMPTY + st), ph ^ 1u, w, kCodeProducerEmpty)) break;
@@ -305,14 +319,14 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb,
                     pn * L::PANEL_ELEMS, key0, t.bh);
     }
-    ++issued;
+    next = i + STEP;
   }
   if (*w.abort_flag) {
     // Let every copy this thread started land before the CTA exits.
 #pragma unroll
     for (int q = 0; q < L::NQ; ++q)
-      if (t.nkv[q] > 0) drain_phase(bar(L::B_QFULL + q), 0u, w, kCodeDrain);
-    for (int i = max(0, issued - L::STAGES); i < issued; ++i)
+      if (t.nkv[q] > 0 && par == 0) drain_phase(bar(L::B_QFULL + q), 0u, w, kCodeDrain);
+    for (int i = max(par, next - L::STAGES); i < next; i += STEP)
       drain_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u, w,
                   kCodeDrain);
   }
@@ -799,8 +813,10 @@ __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
     __syncthreads();
   } else {
     if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
-    if (warp == L::TMA_WARP) {
-      if (lane == 0) producer_role<D, CAUSAL, SPLIT, F8>(&tm_q, &tm_k, &tm_v, sbase, t, w);
+    if (warp == L::TMA_WARP || (L::SPLIT_LOAD && warp == L::V_WARP)) {
+      if (lane == 0)
+        producer_role<D, CAUSAL, SPLIT, F8>(&tm_q, &tm_k, &tm_v, sbase, t, w,
+                                            warp == L::TMA_WARP ? 0 : 1);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
       mma_role<D, CAUSAL, SPLIT, F8>(tmem, sbase, t, w);
