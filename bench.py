@@ -42,6 +42,14 @@ from exact_attention_51_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (bf16, causal/non-causal) and % of GB300 dense BF16 peak"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# The GB300 dense bf16 figure from NVIDIA's specification, reported beside the
+# measured peak (which the roofline uses).
+SPEC_BF16_TFLOPS = 2500.0
+SPEC_SOURCE = ("NVIDIA GB300 NVL72 specification: 360 PFLOP/s bf16 with 2:4 sparsity "
+               "/ 72 GPUs / 2 (dense)")
+# Length of the untimed soak before the timed region, and of the default
+# timed region.
+SOAK_S = 1.0
 # The sources that build the bf16 forward kernel this benchmark times: a
 # committed DRAM-traffic figure is used only while they hash to what was
 # profiled.
@@ -430,6 +438,17 @@ def run_ours(args, w, causal):
     st, detail = ea.attn_fwd_device_status()
     if st != ea.ATTN_OK:
         raise RuntimeError(f"device wait timed out during warm-up (code {detail:#x})")
+    # the length of one step, to size the soak and the default step count
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream)
+    for _ in range(3):
+        step()
+    ev_b.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = reduce_max_over_ranks([max(ev_a.elapsed_time(ev_b) / 3, 1e-3)], dev)[0]
+    if args.steps is None:  # default: a timed region of about SOAK_S
+        args.steps = min(1000, max(20, int(math.ceil(SOAK_S * 1e3 / est_ms))))
+    soak_steps = min(20000, int(math.ceil(args.soak_seconds * 1e3 / est_ms)))
 
     # Inputs and outputs smaller than twice L2 would be served from L2 on
     # repeated launches: then every step is timed on its own, after a write
@@ -440,6 +459,14 @@ def run_ours(args, w, causal):
     sampler = ClockSampler(gpu_id_for(local))
     time.sleep(0.3)  # let nvidia-smi start printing
     per_step = []
+    # Untimed soak right before the timed region: about SOAK_S of back-to-back
+    # steps, so that the timed steps start at the clocks and power of a
+    # sustained run and the clock samples cover more than a few steps.
+    barrier()
+    t_soak0 = time.monotonic()
+    for _ in range(soak_steps):
+        step()
+    torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     t_host0 = time.monotonic()
@@ -467,6 +494,7 @@ def run_ours(args, w, causal):
     time.sleep(0.1)
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
+    clocks_soak = sampler.summary(t_soak0, t_host0)
     if not flush:
         # step-by-step spread, outside the timed region above
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -563,6 +591,11 @@ def run_ours(args, w, causal):
                        "parallelism": f"replicas x{ws} (independent batches, no collective)",
                        "kv_splits": path.splits},
             "pct_of_peak": 100.0 * achieved / peak,
+            "pct_of_spec_peak": 100.0 * achieved / (SPEC_BF16_TFLOPS * path.peak_mult),
+            "spec_peak": {"tflops": SPEC_BF16_TFLOPS * path.peak_mult,
+                          "frac": achieved / (SPEC_BF16_TFLOPS * path.peak_mult),
+                          "source": SPEC_SOURCE + (" x 2 (fp8 : bf16)" if path.peak_mult == 2.0
+                                                   else "")},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "traffic": traffic,
@@ -576,6 +609,8 @@ def run_ours(args, w, causal):
                     "frac": w.min_hbm_bytes() / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                     "peak_source": f"{peak_src} copy"} if path.name == "fwd" else None,
             "clocks": clocks,
+            "soak": {"steps": soak_steps, "seconds": t_host0 - t_soak0, "clocks": clocks_soak,
+                     "what": "untimed back-to-back steps right before the timed region"},
             "e2e": {"value": whole_job_tflops(path.flops, ws, e2e_ms), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
@@ -605,12 +640,15 @@ def run_ours(args, w, causal):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: as many as fill about one second, at least 20)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--causal", choices=["default", "0", "1"], default="default")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--soak-seconds", type=float, default=SOAK_S,
+                    help="untimed back-to-back steps right before the timed region (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fwd", "fp8", "bwd"], default="fwd",
                     help="fwd: attn_fwd (bf16, the headline); fp8: attn_fwd_fp8 on the "
@@ -628,6 +666,8 @@ def main(argv=None):
     if args.path == "bwd" and w.d not in (64, 128):
         ap.error("--path bwd needs a d = 64 or 128 workload")
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
         if args.path != "fwd":
             ap.error("--impl reference times the forward oracle only")
         return run_reference(args, w, causal)

@@ -36,6 +36,7 @@ ATTN_ERR_NOALLOC_TOO_LARGE = 7
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024  # ATTN_NOALLOC_WORKSPACE_BYTES
 
 SUPPORTED_HEAD_DIMS = (64, 128, 256)
+FP8_HEAD_DIMS = (128, 256)  # head dims of attn_fwd_fp8 / attn_fwd_fp8_kvcache
 
 _lock = threading.Lock()
 _lib = None
@@ -108,6 +109,9 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_fp8_kvcache_num_splits.restype = _int
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
         lib.attn_selftest_wait_timeout.restype = _int
+        lib.attn_selftest_fwd_dropped_load.argtypes = [_vp, _vp, _vp, _vp, _vp, _int, _int, _int,
+                                                       _int, _flt, _int, _int, ctypes.c_uint, _vp]
+        lib.attn_selftest_fwd_dropped_load.restype = _int
         _lib = lib
         return lib
 
@@ -463,6 +467,26 @@ def attn_selftest_wait_timeout(timeout_ms: int = 100, stream=None, device=None) 
     with torch.cuda.device(device):
         return int(load_library().attn_selftest_wait_timeout(int(timeout_ms),
                                                              _stream_handle(stream, device)))
+
+
+def attn_selftest_fwd_dropped_load(q, k, v, out, lse, causal: bool, drop_load: int,
+                                   timeout_ms: int = 50, scale: float | None = None,
+                                   stream=None) -> int:
+    """Enqueue the forward's abort-path self-test (see include/attn_fwd.h):
+    attn_fwd on these tensors with the copy of ring position ``drop_load``
+    left out and every wait limited to ``timeout_ms``.  Returns the C status;
+    the outcome is read with ``attn_fwd_device_status``."""
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse = _outputs(q, out, lse)
+    with torch.cuda.device(q.device):
+        return int(load_library().attn_selftest_fwd_dropped_load(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), int(drop_load), int(timeout_ms),
+            _stream_handle(stream, q.device)))
 
 
 def attn_fwd_device_status(stream=None, device=None):

@@ -156,6 +156,11 @@ unsigned int* status_word() {
   DeviceState* ds = nullptr;
   return device_state(&ds) == ATTN_OK ? ds->status : nullptr;
 }
+int device_ready() {
+  DeviceState* ds = nullptr;
+  return device_state(&ds);
+}
+int record_cuda_error(cudaError_t e) { return fail_cuda(e); }
 }  // namespace ea51
 
 extern "C" {
@@ -178,7 +183,8 @@ ea51::FwdVariant variant_for(int d) {
 // kernel writes partials to o_part / lse_part.
 int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int Nq, int Nk, int d, float scale, int causal, int kv_splits, float* o_part,
-               float* lse_part, DeviceState* ds, cudaStream_t stream) {
+               float* lse_part, DeviceState* ds, cudaStream_t stream, int drop_load = -1,
+               unsigned long long wait_timeout_ns = 0) {
   const ea51::FwdVariant var = variant_for(d);
   const int64_t BH = static_cast<int64_t>(B) * H;
   alignas(64) CUtensorMap tq, tk, tv;
@@ -204,12 +210,14 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   p.kv_splits = kv_splits;
   p.o_part = o_part;
   p.lse_part = lse_part;
+  p.drop_load = drop_load;
+  p.wait_timeout_ns = wait_timeout_ns;
   const cudaError_t e = var.launch(&tq, &tk, &tv, p, causal != 0, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTN_OK;
 }
 
-constexpr int kMaxSplits = 64;
+constexpr int kMaxSplits = ea51::kMaxKvSplits;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -590,6 +598,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   return ATTN_OK;
 }
 
+
+int attn_selftest_fwd_dropped_load(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int N, int d, float scale, int causal,
+                                   int drop_load, unsigned int timeout_ms, void* stream) {
+  if (drop_load < 0 || timeout_ms < 1 || timeout_ms > 10000) return ATTN_ERR_INVALID_ARG;
+  int rc = check_general(q, k, v, o, lse, B, H, N, N, d, scale, causal);
+  if (rc != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  return launch_fwd(q, k, v, o, lse, B, H, N, N, d, scale, causal, 1, nullptr, nullptr, ds,
+                    static_cast<cudaStream_t>(stream), drop_load,
+                    static_cast<unsigned long long>(timeout_ms) * 1000000ull);
+}
 
 int attn_selftest_wait_timeout(unsigned int timeout_ms, void* stream) {
   if (timeout_ms < 1 || timeout_ms > 10000) return ATTN_ERR_INVALID_ARG;

@@ -5,7 +5,10 @@
 // (the associative merge of per-block softmax states, "algebraic aggregates"
 // in HN item 40939030; the online-softmax rescaling of "Tri Dao: prediction"
 // applied across CTAs instead of across tiles).  Splits with L_s = -inf saw no
-// key and are skipped.  One warp per row; HBM-bound.
+// key and are skipped.  Every row the entry points accept sees at least one
+// key (causal rows need Nk >= Nq), so some split of it is non-empty; a row
+// whose splits were all empty would be written as O = 0, LSE = -inf (the
+// empty sum) rather than as 0/0.  One warp per row; HBM-bound.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -44,12 +47,12 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
       acc[e + 1] += wgt * v.y;
     }
   }
-  const float inv = 1.f / wsum;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   __nv_bfloat16* dst = o + row * D + lane * PER;
 #pragma unroll
   for (int e = 0; e < PER; e += 2)
     *reinterpret_cast<__nv_bfloat162*>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-  if (lane == 0) lse[row] = m + logf(wsum);
+  if (lane == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 }  // namespace

@@ -154,11 +154,13 @@ struct Layout {
 struct Waiter {
   volatile uint32_t* abort_flag;  // shared memory, CTA-wide
   unsigned int* status;           // global, device-wide
+  unsigned long long timeout_ns = kWaitTimeoutNs;  // limit of each wait
 };
 
+// `timeout_ns` 0: the waiter's own limit.
 static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, Waiter w, uint32_t code,
-                                       bool honour_abort,
-                                       unsigned long long timeout_ns = kWaitTimeoutNs) {
+                                       bool honour_abort, unsigned long long timeout_ns = 0) {
+  if (timeout_ns == 0) timeout_ns = w.timeout_ns;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
@@ -273,6 +275,9 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
 }
 
 // One lane runs this and loads Q, then K_0, V_0, K_1, ... in ring order.
+// `drop_load` (a test hook, -1 on every product path) names a ring position
+// whose copy is not issued: nothing arrives on its full barrier, so the MMA
+// warp's bounded wait for it runs out and the CTA takes its abort path.
 // With SPLIT_LOAD, lanes of two warps run it: `par` = 0 loads Q and the K
 // tiles (even ring positions), `par` = 1 the V tiles (odd positions); with an
 // even number of ring slots K and V use disjoint slots, so a K tile is never
@@ -281,7 +286,7 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
 template <int D, bool CAUSAL, bool SPLIT, bool F8>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
-                              Waiter w, int par) {
+                              Waiter w, int par, int drop_load) {
   using L = Layout<D, F8>;
   static_assert(!L::SPLIT_LOAD || L::STAGES % 2 == 0, "K and V take alternate ring slots");
   constexpr int STEP = L::SPLIT_LOAD ? 2 : 1;
@@ -306,6 +311,8 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     const int st = i % L::STAGES;
     const uint32_t ph = static_cast<uint32_t>(i / L::STAGES) & 1u;
     if (!wait_phase(bar(L::B_KVEMPTY + st), ph ^ 1u, w, kCodeProducerEmpty)) break;
+    next = i + STEP;
+    if (i == drop_load) continue;  // test hook: this slot never fills
     const uint32_t fb = bar(L::B_KVFULL + st);
     mbar_arrive_expect_tx(fb, L::KV_BYTES);
     const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
@@ -319,7 +326,6 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb,
                     pn * L::PANEL_ELEMS, key0, t.bh);
     }
-    next = i + STEP;
   }
   if (*w.abort_flag) {
     // Let every copy this thread started land before the CTA exits.
@@ -327,8 +333,9 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     for (int q = 0; q < L::NQ; ++q)
       if (t.nkv[q] > 0 && par == 0) drain_phase(bar(L::B_QFULL + q), 0u, w, kCodeDrain);
     for (int i = max(par, next - L::STAGES); i < next; i += STEP)
-      drain_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u, w,
-                  kCodeDrain);
+      if (i != drop_load)
+        drain_phase(bar(L::B_KVFULL + i % L::STAGES), static_cast<uint32_t>(i / L::STAGES) & 1u,
+                    w, kCodeDrain);
   }
 }
 
@@ -778,7 +785,7 @@ __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
   const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8>(p);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
-  const Waiter w{abort_flag, p.status};
+  const Waiter w{abort_flag, p.status, p.wait_timeout_ns ? p.wait_timeout_ns : kWaitTimeoutNs};
 
   if (threadIdx.x == 0) {
     const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -816,7 +823,7 @@ __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
     if (warp == L::TMA_WARP || (L::SPLIT_LOAD && warp == L::V_WARP)) {
       if (lane == 0)
         producer_role<D, CAUSAL, SPLIT, F8>(&tm_q, &tm_k, &tm_v, sbase, t, w,
-                                            warp == L::TMA_WARP ? 0 : 1);
+                                            warp == L::TMA_WARP ? 0 : 1, p.drop_load);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
       mma_role<D, CAUSAL, SPLIT, F8>(tmem, sbase, t, w);

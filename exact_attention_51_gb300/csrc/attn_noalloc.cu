@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "attn_fwd.h"
+#include "fwd_dispatch.h"
 
 namespace {
 
@@ -36,13 +37,20 @@ void* g_addr[kMaxDevices] = {};  // device address of the array, per device
 extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                                         float* lse, int B, int H, int N, int d, float scale,
                                         int causal, int num_splits, void* stream) {
-  if (num_splits > 1) {
-    const size_t need = attn_fwd_splitkv_workspace_size(B, H, N, d, num_splits);
-    if (need == 0) return ATTN_ERR_INVALID_ARG;  // sizes attn_fwd_splitkv would reject
-    if (need > ATTN_NOALLOC_WORKSPACE_BYTES) return ATTN_ERR_NOALLOC_TOO_LARGE;
-  }
+  // The checks attn_fwd_splitkv makes, in its order, so that both entry
+  // points answer the same arguments with the same status; the size limit of
+  // the fixed array comes before anything touches the device.
+  int rc = attn_fwd_check_args(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > ea51::kMaxKvSplits) return ATTN_ERR_INVALID_ARG;
+  if (num_splits > 1 &&
+      attn_fwd_splitkv_workspace_size(B, H, N, d, num_splits) > ATTN_NOALLOC_WORKSPACE_BYTES)
+    return ATTN_ERR_NOALLOC_TOO_LARGE;
+  if ((rc = ea51::device_ready()) != ATTN_OK) return rc;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_LAUNCH;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return ea51::record_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED_DEVICE;
   void* ws = nullptr;
   {
     // One-time set-up per device, with that device current: the host-side
@@ -51,8 +59,9 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_addr[dev]) {
       void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_noalloc_workspace) != cudaSuccess || !addr)
-        return ATTN_ERR_LAUNCH;
+      if ((e = cudaGetSymbolAddress(&addr, g_noalloc_workspace)) != cudaSuccess)
+        return ea51::record_cuda_error(e);
+      if (!addr) return ea51::record_cuda_error(cudaErrorInvalidSymbol);
       g_addr[dev] = addr;
     }
     ws = g_addr[dev];

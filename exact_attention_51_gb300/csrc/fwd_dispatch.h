@@ -25,6 +25,10 @@ struct FwdParams {
   int kv_splits;
   float* o_part;
   float* lse_part;
+  // Test hook of attn_selftest_fwd_dropped_load, -1 on every other path: the
+  // K/V ring position whose copy the producer leaves out in every CTA.
+  int drop_load = -1;
+  unsigned long long wait_timeout_ns = 0;  // limit of each bounded wait (0: about 2 s)
 };
 
 struct FwdVariant {
@@ -41,6 +45,18 @@ cudaError_t launch_combine(int d, const float* o_part, const float* lse_part, vo
 // Device address of the current device's wait-timeout status word (set up by
 // the C ABI's per-device initialisation; nullptr if that failed).
 unsigned int* status_word();
+
+// Largest key-split count of the split-KV entry points.
+constexpr int kMaxKvSplits = 64;
+
+// The per-device set-up and check of every entry point (compute capability
+// 10.3, status word, tensor-map encoder): ATTN_OK or the status the entry
+// point returns.  For entry points defined outside attn_api.cu.
+int device_ready();
+
+// Records `e` as this host thread's last CUDA error (attn_last_cuda_error)
+// and returns ATTN_ERR_LAUNCH.
+int record_cuda_error(cudaError_t e);
 
 // Launches a one-block kernel that waits on an mbarrier nothing arrives on,
 // with the kernel's bounded wait cut to `timeout_ns`.

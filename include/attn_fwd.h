@@ -87,6 +87,14 @@ enum attn_status {
  * Enqueues one kernel and returns.  On any validation error nothing is
  * launched and the status says why.  O rows are the probability-weighted
  * value rows rounded to bf16 (round to nearest even); LSE is fp32.
+ *
+ * One thread block owns 256 query rows of one head (128 for d = 256), so a
+ * launch has B*H*ceil(N/256) blocks.  When that is below the number of
+ * multiprocessors (152 on GB300) -- few heads, long rows, as in decoding or
+ * B=1 H=4 N=8192 -- part of the GPU idles; attn_fwd_splitkv with the count
+ * from attn_fwd_splitkv_num_splits shares each block's keys over several
+ * blocks instead (measured on B=1 H=4 N=8192 d=128 causal: 627 TFLOP/s here,
+ * 848 with 2 splits).  For launches of a wave or more, attn_fwd is faster.
  */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, void* stream);
@@ -224,6 +232,31 @@ ATTN_API int attn_last_cuda_error(void);
  * device, so run this only when no other launch of the library is in flight.
  */
 ATTN_API int attn_selftest_wait_timeout(unsigned int timeout_ms, void* stream);
+
+/*
+ * Self-test of the fused kernel's own abort path (a test hook, not a way to
+ * compute attention): runs attn_fwd on the given arguments, except that in
+ * every thread block the TMA producer leaves out the copy of K/V ring
+ * position `drop_load` (0 = K tile 0, 1 = V tile 0, 2 = K tile 1, ...) and
+ * every bounded wait gives up after `timeout_ms` (1..10000) milliseconds.
+ * Nothing arrives on that slot's barrier, so the MMA warp's wait for it (or a
+ * wait that depends on it: the producer's for a free slot, the softmax's for
+ * the next scores) runs out: the first to give up records its code (0x1xx:
+ * 0x101 producer, 0x11x MMA warp, 0x12x softmax) in the device status word
+ * and raises the block's abort flag; the other roles leave their waits, every
+ * role lets the copies and tensor-core operations it started finish (bounded
+ * again), tensor memory is freed and the kernel returns.  Blocks that see fewer ring
+ * positions than `drop_load` run to the end as usual.  O and LSE are not
+ * valid afterwards; attn_fwd_device_status returns ATTN_ERR_TIMEOUT with the
+ * code and clears the word, and the CUDA context stays usable.  Arguments
+ * and errors as attn_fwd, plus ATTN_ERR_INVALID_ARG for drop_load < 0 or a
+ * limit out of range.  The status word is shared with every launch of the
+ * library on the device, so run this only when no other is in flight.
+ */
+ATTN_API int attn_selftest_fwd_dropped_load(const void* q, const void* k, const void* v, void* o,
+                                            float* lse, int B, int H, int N, int d, float scale,
+                                            int causal, int drop_load, unsigned int timeout_ms,
+                                            void* stream);
 
 #ifdef __cplusplus
 }

@@ -40,6 +40,13 @@ import torch
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
+# Comparisons of two calls that compute every row with the same fp64
+# operations are exact for the C oracle.  An implementation built on library
+# matrix products groups its sums by the problem's shape, so where the two
+# calls differ in shape it may differ in the last bits: such a caller raises
+# this (the dense oracle's tests use 1e-13).
+SHAPE_REGROUP_ATOL = 0.0
+
 
 def _rng(seed):
     return np.random.default_rng(seed)
@@ -358,8 +365,10 @@ def pin_bottom_right_suffix(orc):
         qf, k, v = (r.standard_normal((1, 2, Nk, 6)) for _ in range(3))
         o_full, lse_full = orc.attn_f64(qf, k, v, True, 0.8)
         o, lse = orc.attn_f64_qk(qf[:, :, Nk - Nq:], k, v, True, 0.8)
-        fails += _close(f"bottom-right O Nq={Nq} Nk={Nk}", o, o_full[:, :, Nk - Nq:], 0.0)
-        fails += _close(f"bottom-right lse Nq={Nq} Nk={Nk}", lse, lse_full[:, :, Nk - Nq:], 0.0)
+        fails += _close(f"bottom-right O Nq={Nq} Nk={Nk}", o, o_full[:, :, Nk - Nq:],
+                        SHAPE_REGROUP_ATOL)
+        fails += _close(f"bottom-right lse Nq={Nq} Nk={Nk}", lse, lse_full[:, :, Nk - Nq:],
+                        SHAPE_REGROUP_ATOL)
     return fails
 
 

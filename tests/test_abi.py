@@ -299,3 +299,23 @@ def test_fp8_kvcache_rejects_bad_arguments(lib):
     assert f(1, 2, 16, 4096, 128, 4) > f(1, 2, 16, 4096, 128, 1)
     assert f(1, 2, 16, 4096, 64, 1) == 0
     assert ea.load_library().attn_fwd_fp8_kvcache_num_splits(1, 8, 1, 32768, 128, 1, 152) >= 2
+
+
+def _noalloc(lib, p, B, H, N, d, splits, causal=0, scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd_splitkv_noalloc(vp(p[0]), vp(p[1]), vp(p[2]), vp(p[3]), vp(p[4]), B, H, N,
+                                        d, ctypes.c_float(scale), causal, splits, None)
+
+
+def test_noalloc_host_checks_come_before_the_device(lib):
+    """attn_fwd_splitkv_noalloc answers bad arguments, a split count out of
+    range and a problem beyond its fixed array before it touches the device
+    (these run without a GPU)."""
+    n = 1 * 64 * 8192 * 128 * 2
+    p = ptrs(n)
+    assert _noalloc(lib, p, 1, 64, 8192, 128, 4) == ea.ATTN_ERR_NOALLOC_TOO_LARGE
+    for splits in (0, -3, 65):
+        assert _noalloc(lib, p, 1, 2, 128, 64, splits) == ea.ATTN_ERR_INVALID_ARG
+    assert _noalloc(lib, p, 1, 2, 128, 96, 2) == ea.ATTN_ERR_INVALID_ARG      # d
+    assert _noalloc(lib, [A + 2] + p[1:], 1, 2, 128, 64, 2) == ea.ATTN_ERR_MISALIGNED
+    assert _noalloc(lib, p, 1, 2, 128, 64, 2, scale=-1.0) == ea.ATTN_ERR_INVALID_ARG
