@@ -363,19 +363,20 @@ def make_path(args, w, causal, ea, dev):
         return p
     if args.path == "fp8":
         q8, k8, v8, sc = wl.make_inputs_e4m3(w.B, w.H, w.N, w.d, w.dist, w.seed, w.k_outlier_frac)
-        ws_bytes = ea.attn_fwd_fp8_workspace_size(w.B, w.H, w.N, w.d)
+        ws_bytes = ea.attn_fwd_fp8_workspace_size(w.B, w.H, w.N, w.d)  # > 0: V read transposed
 
         def call(i, o, scratch, st):
             ea.attn_fwd_fp8(i["q"], i["k"], i["v"], *sc, causal=causal, out=o["o"], lse=o["lse"],
                             workspace=scratch, stream=st)
         p = BenchPath("fp8", "attention fwd TFLOP/s (e4m3 Q/K/V, per-tensor scales) and % of "
-                      "GB300 dense FP8 peak", "e4m3", w.flops(causal), 2,
-                      f"attn_fwd_kernel<{w.d},{str(causal).lower()},e4m3> + V transpose",
+                      "GB300 dense FP8 peak", "e4m3", w.flops(causal), 2 if ws_bytes else 1,
+                      f"attn_fwd_kernel<{w.d},{str(causal).lower()},e4m3>"
+                      + (" + V transpose" if ws_bytes else ""),
                       2.0,  # dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s nominal)
                       {"q": q8, "k": k8, "v": v8},
                       lambda d: {"o": torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=d),
                                  "lse": torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=d)},
-                      lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
+                      lambda d: torch.empty(ws_bytes, dtype=torch.uint8, device=d) if ws_bytes else None,
                       call, ["o", "lse"])
         p.splits = 1
         return p
@@ -661,8 +662,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     w = wl.WORKLOADS[args.workload]
     causal = w.causal[-1] if args.causal == "default" else args.causal == "1"
-    if args.path == "fp8" and w.d not in (128, 256):
-        ap.error("--path fp8 needs a d = 128 or 256 workload")
+    if args.path == "fp8" and w.d not in (64, 128, 256):
+        ap.error("--path fp8 needs a d = 64, 128 or 256 workload")
     if args.path == "bwd" and w.d not in (64, 128):
         ap.error("--path bwd needs a d = 64 or 128 workload")
     if args.impl == "reference":

@@ -36,7 +36,7 @@ ATTN_ERR_NOALLOC_TOO_LARGE = 7
 NOALLOC_WORKSPACE_BYTES = 64 * 1024 * 1024  # ATTN_NOALLOC_WORKSPACE_BYTES
 
 SUPPORTED_HEAD_DIMS = (64, 128, 256)
-FP8_HEAD_DIMS = (128, 256)  # head dims of attn_fwd_fp8 / attn_fwd_fp8_kvcache
+FP8_HEAD_DIMS = (64, 128, 256)  # head dims of attn_fwd_fp8 / attn_fwd_fp8_kvcache
 
 _lock = threading.Lock()
 _lib = None
@@ -177,6 +177,13 @@ def _outputs(q, out, lse):
     return out, lse
 
 
+def _buffer(t):
+    """(device pointer, bytes) of an optional scratch tensor; (None, 0) for none."""
+    if t is None:
+        return None, 0
+    return t.data_ptr(), t.numel() * t.element_size()
+
+
 def attn_fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().attn_fwd_fp8_workspace_size(B, H, N, d))
 
@@ -184,10 +191,11 @@ def attn_fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
 def attn_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
                  causal: bool = False, scale: float | None = None, out=None, lse=None,
                  workspace=None, stream=None):
-    """Attention forward on e4m3 inputs: q, k, v CUDA tensors [B, H, N, d], d = 128 or 256,
-    of dtype float8_e4m3fn (or uint8 holding e4m3 codes), element x meaning
-    ``descale * x``.  Returns ``(o, lse)``: o bf16 [B,H,N,d], lse fp32
-    [B,H,N].  The V-transpose workspace is allocated with torch unless
+    """Attention forward on e4m3 inputs: q, k, v CUDA tensors [B, H, N, d], d = 64, 128
+    or 256, of dtype float8_e4m3fn (or uint8 holding e4m3 codes), element x
+    meaning ``descale * x``.  Returns ``(o, lse)``: o bf16 [B,H,N,d], lse fp32
+    [B,H,N].  A workspace, if the call needs one
+    (``attn_fwd_fp8_workspace_size``), is allocated with torch unless
     given."""
     import torch
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -214,14 +222,14 @@ def attn_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float,
             or lse.device != q.device:
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor on q's device")
     need = attn_fwd_fp8_workspace_size(B, H, N, d)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = _buffer(workspace)
     with torch.cuda.device(q.device):
         rc = load_library().attn_fwd_fp8(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
             float(descale_v), out.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
-            int(bool(causal)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-            _stream_handle(stream, q.device))
+            int(bool(causal)), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
     return out, lse
@@ -231,7 +239,7 @@ def attn_fwd_fp8_kvcache(q, k, v, descale_q: float, descale_k: float, descale_v:
                          causal: bool = False, scale: float | None = None,
                          num_splits: int | None = None, out=None, lse=None, workspace=None,
                          stream=None):
-    """e4m3 forward with q [B,H,Nq,d] and k, v [B,H,Nk,d] (d = 128 or 256):
+    """e4m3 forward with q [B,H,Nq,d] and k, v [B,H,Nk,d] (d = 64, 128 or 256):
     the queries are the last Nq positions (causal diagonal at the
     bottom-right).  ``num_splits`` None picks one from the shape and the SM
     count.  Returns ``(o, lse)`` as attn_fwd_fp8."""
@@ -266,14 +274,14 @@ def attn_fwd_fp8_kvcache(q, k, v, descale_q: float, descale_k: float, descale_v:
             or lse.device != q.device:
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor on q's device")
     need = int(lib.attn_fwd_fp8_kvcache_workspace_size(B, H, Nq, Nk, d, num_splits))
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = _buffer(workspace)
     with torch.cuda.device(q.device):
         rc = lib.attn_fwd_fp8_kvcache(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
             float(descale_v), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d, float(scale),
-            int(bool(causal)), int(num_splits), workspace.data_ptr(),
-            workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+            int(bool(causal)), int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8_kvcache")
     return out, lse

@@ -122,20 +122,24 @@ int device_state(DeviceState** out) {
 }
 
 // A [BH, rows, cols] tensor (cols innermost, `pitch` elements between rows)
-// with a box of 128 bytes of columns x `box_rows` rows x one head, 128-byte
-// swizzle.  Rows and columns past the extents read as zeros, so a ragged last
-// tile never touches the next head.
+// with a box of one swizzle span of columns x `box_rows` rows x one head:
+// `swz` = 128 bytes with 128-byte swizzle, or 64 bytes with 64-byte swizzle
+// (the kernel's Layout::SWZ).  Rows and columns past the extents read as
+// zeros, so a ragged last tile never touches the next head.
 int encode_tiled(CUtensorMap* map, const void* base, CUtensorMapDataType type, int elem_bytes,
-                 int64_t BH, int64_t rows, int64_t cols, int64_t pitch, int box_rows) {
+                 int64_t BH, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                 int swz = 128) {
+  const bool narrow = swz == 64;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch * elem_bytes),
                                  static_cast<cuuint64_t>(pitch * elem_bytes * rows)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes),
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>((narrow ? 64 : 128) / elem_bytes),
                              static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = g_encode(map, type, 3, const_cast<void*>(base), dims, strides, box, estride,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     t_last_cuda_error = static_cast<int>(r);
@@ -174,9 +178,17 @@ int attn_fwd_check_args(const void* q, const void* k, const void* v, const void*
 
 namespace {
 
-ea51::FwdVariant variant_for(int d) {
-  return d == 64 ? ea51::fwd_variant_d64() : d == 128 ? ea51::fwd_variant_d128()
-                                                      : ea51::fwd_variant_d256();
+// Keys per head up to which head dims 64 and 128 run the two-CTAs-per-SM
+// shape (one query tile per CTA): with few key tiles per query tile, the
+// per-CTA set-up and epilogue weigh more than sharing K/V between two query
+// tiles saves.
+constexpr int kTwoCtaMaxKeys = 2048;
+
+ea51::FwdVariant variant_for(int d, int Nk) {
+  if (d == 64) return Nk <= kTwoCtaMaxKeys ? ea51::fwd_variant_d64_two() : ea51::fwd_variant_d64();
+  if (d == 128)
+    return Nk <= kTwoCtaMaxKeys ? ea51::fwd_variant_d128_two() : ea51::fwd_variant_d128();
+  return ea51::fwd_variant_d256();
 }
 
 // Encodes the TMA maps and launches the fused kernel; with kv_splits > 1 the
@@ -185,7 +197,7 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, int causal, int kv_splits, float* o_part,
                float* lse_part, DeviceState* ds, cudaStream_t stream, int drop_load = -1,
                unsigned long long wait_timeout_ns = 0) {
-  const ea51::FwdVariant var = variant_for(d);
+  const ea51::FwdVariant var = variant_for(d, Nk);
   const int64_t BH = static_cast<int64_t>(B) * H;
   alignas(64) CUtensorMap tq, tk, tv;
   int rc;
@@ -281,7 +293,7 @@ int split_model(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1)
     return 1;
   if (causal && Nk < Nq) return 1;
-  return split_model_for(variant_for(d), B, H, Nq, Nk, causal, num_sms);
+  return split_model_for(variant_for(d, Nk), B, H, Nq, Nk, causal, num_sms);
 }
 
 // The model for the tile shape of `var` (query rows per CTA, keys per tile).
@@ -405,15 +417,19 @@ int attn_last_cuda_error(void) { return t_last_cuda_error; }
 
 namespace {
 
+bool fp8_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
 ea51::FwdVariant fp8_variant(int d) {
-  return d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
+  return d == 64 ? ea51::fwd_variant_e4m3_d64()
+                 : d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
 }
 
-// e4m3 workspace: V^T [BH, d, round_up(Nk, 16)] bytes, then (split-KV) the
-// fp32 partial O and LSE; `part_off` receives the partials' offset.
+// e4m3 workspace: (when V is read transposed) V^T [BH, d, round_up(Nk, 16)]
+// bytes, then (split-KV) the fp32 partial O and LSE; `part_off` receives the
+// partials' offset.
 size_t fp8_ws_bytes(int64_t BH, int Nq, int Nk, int d, int splits, size_t* part_off) {
   const size_t nk_pad = (static_cast<size_t>(Nk) + 15) / 16 * 16;
-  const size_t vt = align256(static_cast<size_t>(BH) * d * nk_pad);
+  const size_t vt = ea51::kF8VMnMajor ? 0 : align256(static_cast<size_t>(BH) * d * nk_pad);
   if (part_off) *part_off = vt;
   return vt + (splits > 1 ? splitkv_bytes(BH, Nq, d, splits, nullptr) : 0);
 }
@@ -422,8 +438,8 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
                 float descale_v, void* o, float* lse, int B, int H, int Nq, int Nk, int d,
                 float scale, int causal, int splits, void* workspace, size_t workspace_bytes,
                 void* stream) {
-  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256)) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || !fp8_head_dim(d)) return ATTN_ERR_INVALID_ARG;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
@@ -434,11 +450,12 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
       BH * ((static_cast<int64_t>(Nk) + 127) / 128) > 0x7fffffffLL || Nk > 0x7fffffff - 16)
     return ATTN_ERR_INVALID_ARG;
   const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
-  if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4) || !al(workspace, 256))
-    return ATTN_ERR_MISALIGNED;
   size_t part_off = 0;
   const size_t need = fp8_ws_bytes(BH, Nq, Nk, d, splits, &part_off);
-  if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
+  if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4) ||
+      (need > 0 && !al(workspace, 256)))
+    return ATTN_ERR_MISALIGNED;
   // one byte per e4m3 element
   const size_t q_bytes = static_cast<size_t>(BH) * Nq * d, kv_bytes = static_cast<size_t>(BH) * Nk * d;
   const void* ins[3] = {q, k, v};
@@ -446,25 +463,34 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
   const void* outs[3] = {o, lse, workspace};
   const size_t out_bytes[3] = {q_bytes * 2, static_cast<size_t>(BH) * Nq * 4, need};
   for (int i = 0; i < 3; ++i) {
+    if (out_bytes[i] == 0) continue;
     for (int j = 0; j < 3; ++j)
       if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return ATTN_ERR_ALIAS;
     for (int j = i + 1; j < 3; ++j)
-      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return ATTN_ERR_ALIAS;
+      if (out_bytes[j] > 0 && overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j]))
+        return ATTN_ERR_ALIAS;
   }
   DeviceState* ds = nullptr;
   int rc;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int nk_pad = (Nk + 15) / 16 * 16;
-  cudaError_t e = ea51::launch_transpose_v8(v, workspace, BH, Nk, d, nk_pad, st);
-  if (e != cudaSuccess) return fail_cuda(e);
+  cudaError_t e;
   const ea51::FwdVariant var = fp8_variant(d);
   alignas(64) CUtensorMap tq, tk, tv;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if ((rc = encode_tiled(&tq, q, u8, 1, BH, Nq, d, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_tiled(&tk, k, u8, 1, BH, Nk, d, d, var.kv_rows)) != ATTN_OK) return rc;
-  // V^T [BH, d, nk_pad]: rows are the d columns of V, keys innermost
-  if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, Nk, nk_pad, d)) != ATTN_OK) return rc;
+  const int swz = d >= 128 ? 128 : d;  // one byte per element
+  if ((rc = encode_tiled(&tq, q, u8, 1, BH, Nq, d, d, 128, swz)) != ATTN_OK) return rc;
+  if ((rc = encode_tiled(&tk, k, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
+  if (ea51::kF8VMnMajor) {
+    // V as stored, tiled like K
+    if ((rc = encode_tiled(&tv, v, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
+  } else {
+    const int nk_pad = (Nk + 15) / 16 * 16;
+    e = ea51::launch_transpose_v8(v, workspace, BH, Nk, d, nk_pad, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    // V^T [BH, d, nk_pad]: rows are the d columns of V, keys innermost
+    if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, Nk, nk_pad, d)) != ATTN_OK) return rc;
+  }
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
@@ -501,7 +527,7 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
 extern "C" {
 
 size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 128 && d != 256)) return 0;
+  if (B < 1 || H < 1 || N < 1 || !fp8_head_dim(d)) return 0;
   return fp8_ws_bytes(static_cast<int64_t>(B) * H, N, N, d, 1, nullptr);
 }
 
@@ -513,13 +539,13 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
 }
 
 size_t attn_fwd_fp8_kvcache_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256)) return 0;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || !fp8_head_dim(d)) return 0;
   if (num_splits < 1 || num_splits > kMaxSplits) return 0;
   return fp8_ws_bytes(static_cast<int64_t>(B) * H, Nq, Nk, d, num_splits, nullptr);
 }
 
 int attn_fwd_fp8_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 128 && d != 256) || num_sms < 1) return 1;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || !fp8_head_dim(d) || num_sms < 1) return 1;
   if (causal && Nk < Nq) return 1;
   return split_model_for(fp8_variant(d), B, H, Nq, Nk, causal, num_sms);
 }

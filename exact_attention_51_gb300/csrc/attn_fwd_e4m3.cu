@@ -1,6 +1,6 @@
-// e4m3 (8-bit) inputs, head dims 128 and 256: the fused forward with Q K^T
-// and P V on tcgen05.mma kind::f8f6f4, and the V transpose it reads its P.V
-// operand from.
+// e4m3 (8-bit) inputs, head dims 64, 128 and 256: the fused forward with
+// Q K^T and P V on tcgen05.mma kind::f8f6f4, and the V transpose its P.V
+// operand is read from when V is not read MN-major (kF8VMnMajor).
 #include "launch.cuh"
 
 namespace ea51 {
@@ -69,17 +69,25 @@ cudaError_t launch_e4m3(const CUtensorMap* tq, const CUtensorMap* tk, const CUte
 cudaError_t launch_transpose_v8(const void* v, void* vt, long long BH, int N, int d, int n_pad,
                                 cudaStream_t stream) {
   const long long nblk = (static_cast<long long>(N) + kTKeys - 1) / kTKeys;
-  if ((d != 128 && d != 256) || N < 1 || n_pad % 16 != 0 || n_pad < N || BH < 1 ||
+  if ((d != 64 && d != 128 && d != 256) || N < 1 || n_pad % 16 != 0 || n_pad < N || BH < 1 ||
       BH * nblk > 0x7fffffffLL)
     return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(BH * nblk);
-  if (d == 128)
+  if (d == 64)
+    transpose_v8_kernel<64><<<grid, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
+  else if (d == 128)
     transpose_v8_kernel<128><<<grid, 256, 0, stream>>>(
         static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
   else
     transpose_v8_kernel<256><<<grid, 256, 0, stream>>>(
         static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), N, n_pad, static_cast<int>(nblk));
   return cudaGetLastError();
+}
+
+FwdVariant fwd_variant_e4m3_d64() {
+  using L = Layout<64, true>;
+  return FwdVariant{L::BN, L::NQ * BM, &launch_e4m3<64>};
 }
 
 FwdVariant fwd_variant_e4m3_d128() {

@@ -73,32 +73,55 @@ struct Shape<256> {
 struct ShapeE4M3D256 {
   static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
 };
-template <int D, bool F8>
+// Two CTAs per SM (d = 64, 128): one query tile and one S buffer per CTA, so
+// the two query tiles that take turns on the tensor core come from two CTAs.
+// Each CTA fits half the SM: 128 + D <= 256 tensor-memory columns, and Q plus
+// the K/V ring within 113 KiB of shared memory.  Short rows gain: one CTA's
+// set-up, first loads and epilogue overlap the other CTA's key tiles, and a
+// launch has twice as many, lighter CTAs to balance.
+template <int D>
+struct ShapeTwo {
+  static constexpr int BN = 128, NQ = 1, NSB = 1, STAGES = D == 64 ? 4 : 2;
+};
+template <int D, bool F8, bool TWO>
 struct ShapeOf {
   using T = Shape<D>;
 };
 template <>
-struct ShapeOf<256, true> {
+struct ShapeOf<256, true, false> {
   using T = ShapeE4M3D256;
 };
+template <int D>
+struct ShapeOf<D, false, true> {
+  using T = ShapeTwo<D>;
+};
 
-// F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots);
-// the V tile is then stored transposed (D rows of BN keys) so that both MMAs
-// read K-major operands.
-template <int D, bool F8 = false>
+// F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots).
+// The V tile is read MN-major as stored, or (kF8VMnMajor false) from a
+// transposed copy, D rows of BN keys, as a K-major operand.
+template <int D, bool F8 = false, bool TWO = false>
 struct Layout {
-  using Sh = typename ShapeOf<D, F8>::T;
+  using Sh = typename ShapeOf<D, F8, TWO>::T;
+  static constexpr int MIN_BLOCKS = TWO ? 2 : 1;  // CTAs resident per SM
   static constexpr int EB = F8 ? 1 : 2;  // bytes per Q/K/V element
   static constexpr int BN = Sh::BN, NQ = Sh::NQ, NSB = Sh::NSB,
                        STAGES = F8 ? 2 * Sh::STAGES : Sh::STAGES;
-  static constexpr int PANELS = D * EB / 128;  // 128-byte column panels per Q/K row
-  static constexpr int PANEL_ELEMS = 128 / EB;
+  // Rows of Q, K and V tiles are split into column panels of SWZ bytes, each
+  // swizzled over that span (128 bytes; 64 for the 64-byte rows of e4m3 at
+  // d = 64); 8 rows of a panel form one swizzle atom of SBO bytes.
+  static constexpr int SWZ = D * EB >= 128 ? 128 : D * EB;
+  static constexpr int PANELS = D * EB / SWZ;  // column panels per Q/K/V row
+  static constexpr int PANEL_ELEMS = SWZ / EB;
+  static constexpr int SBO = 8 * SWZ;
+  static constexpr int KPP = SWZ / 32;            // 32-byte K-steps per panel
   static constexpr int KSTEPS_QK = D * EB / 32;   // 32-byte K-steps of S = Q K^T
   static constexpr int KSTEPS_PV = BN * EB / 32;  // and of O += P V
+  static constexpr int KEYS_PER_KSTEP = 32 / EB;  // rows of V one P.V K-step reads
+  static constexpr bool VT = F8 && !kF8VMnMajor;  // V tile stored transposed
   static constexpr bool SPLIT_P = BN >= 128;  // hand P to the MMA warp in two halves
-  static constexpr int Q_PANEL = BM * 128;
+  static constexpr int Q_PANEL = BM * SWZ;
   static constexpr int Q_BYTES = BM * D * EB;
-  static constexpr int KV_PANEL = BN * 128;
+  static constexpr int KV_PANEL = BN * SWZ;
   static constexpr int KV_BYTES = BN * D * EB;
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_Q = 0;
@@ -118,8 +141,8 @@ struct Layout {
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
-  // tensor memory columns (fp32 each)
-  static constexpr int TMEM_COLS = 512;
+  // tensor memory columns (fp32 each): all 512, or half for two CTAs per SM
+  static constexpr int TMEM_COLS = 512 / MIN_BLOCKS;
   __host__ __device__ static constexpr int s_col(int q, int b) { return (q * NSB + b) * BN; }
   __host__ __device__ static constexpr int o_col(int q) { return NQ * NSB * BN + q * D; }
   // warps: [0, 4*NQ) softmax warpgroups, then TMA, MMA, two spare warps
@@ -134,18 +157,23 @@ struct Layout {
   // 384 threads launch with 168 registers each (65536 / 384, rounded down to
   // 8).  The control warpgroup drops to 64 and the two softmax warpgroups
   // rise to 208: 2 * 128 * (208 - 168) = 10240 <= 128 * (168 - 64) = 13312.
-  static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
-  static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : 0;
-  static constexpr int REG_CONTROL = NQ == 2 ? 64 : 0;
+  // Two CTAs of 256 threads per SM launch with 128 each: control 56, softmax
+  // 200, 128 * (200 - 128) = 9216 <= 128 * (128 - 56) = 9216.
+  static constexpr int LAUNCH_REGS = (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8 > 255
+                                         ? 255
+                                         : (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8;
+  static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : TWO ? 200 : 0;
+  static constexpr int REG_CONTROL = NQ == 2 ? 64 : TWO ? 56 : 0;
   static_assert(REG_SOFTMAX == 0 ||
                     NQ * 128 * (REG_SOFTMAX - LAUNCH_REGS) <= 128 * (LAUNCH_REGS - REG_CONTROL),
                 "register split exceeds the launch budget");
 
   static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
-  static_assert(!F8 || ((D == 128 || D == 256) && BN == 128),
-                "e4m3 tiles: d = 128 or 256, 128 keys (one 128-byte row of V^T)");
+  static_assert(!F8 || BN == 128, "e4m3 tiles: 128 keys (one 128-byte row of V^T)");
+  static_assert(D * EB % SWZ == 0 && (SWZ == 128 || SWZ == 64), "row panels");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
-  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+  static_assert(SMEM_ALLOC <= 232448 / MIN_BLOCKS - 1024, "shared memory budget");
+  static_assert(!TWO || (!F8 && NQ == 1 && NSB == 1), "two-CTA shape");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1024-byte tile alignment");
 };
 
@@ -222,9 +250,9 @@ struct Tile {
   int nkv[Shape<D>::NQ];      // key tiles [lo, lo + nkv) visited by each query tile
 };
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
 __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, TWO>;
   static_assert(L::NQ <= Shape<D>::NQ, "tile bookkeeping sized by the bf16 shape");
   Tile<D, CAUSAL, SPLIT> t;
   const int splits = SPLIT ? p.kv_splits : 1;
@@ -283,11 +311,11 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
 // even number of ring slots K and V use disjoint slots, so a K tile is never
 // queued behind a V tile whose slot P.V is still reading (with one K and one
 // V slot, the next K loads during P.V and the next V during the next S).
-template <int D, bool CAUSAL, bool SPLIT, bool F8>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                               Waiter w, int par, int drop_load) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, TWO>;
   static_assert(!L::SPLIT_LOAD || L::STAGES % 2 == 0, "K and V take alternate ring slots");
   constexpr int STEP = L::SPLIT_LOAD ? 2 : 1;
   const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -317,7 +345,7 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     mbar_arrive_expect_tx(fb, L::KV_BYTES);
     const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
     const int key0 = (t.lo + (i >> 1)) * L::BN;
-    if (F8 && (i & 1)) {
+    if (L::VT && (i & 1)) {
       // transposed V: one box of D rows x BN keys (keys innermost)
       tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES, map, fb, key0, 0, t.bh);
     } else {
@@ -342,14 +370,14 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 // Runs on a whole warp with warp-uniform control flow (so the descriptors
 // stay in uniform registers); one elected lane issues every tcgen05.mma and
 // tcgen05.commit.
-template <int D, bool CAUSAL, bool SPLIT, bool F8>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
 __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t, Waiter w) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, TWO>;
   constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
   // A=Q, B=K: both K-major.  A=P (tmem), B=V: MN-major in bf16, K-major for
   // the transposed e4m3 V tile.
   constexpr uint32_t kIdescQK = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
-  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(BM, D) : idesc_bf16_f32(BM, D, true);
+  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(BM, D, !L::VT) : idesc_bf16_f32(BM, D, true);
   auto mma_s = [](uint32_t d_t, uint64_t a, uint64_t b, uint32_t acc, uint32_t issue) {
     if constexpr (F8) mma_ss_f8(d_t, a, b, kIdescQK, acc, issue);
     else mma_ss(d_t, a, b, kIdescQK, acc, issue);
@@ -382,13 +410,13 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
 
   // S(q, b) = Q_q K^T with K in ring slot `ks`
   auto issue_s = [&](int q, int b, int ks) {
-    const uint64_t a0 = sdesc_sw128(sbase + L::OFF_Q + q * L::Q_BYTES, 16, 1024);
-    const uint64_t b0 = sdesc_sw128(slot_addr(ks), 16, 1024);
+    const uint64_t a0 = sdesc_swz<L::SWZ>(sbase + L::OFF_Q + q * L::Q_BYTES, 16, L::SBO);
+    const uint64_t b0 = sdesc_swz<L::SWZ>(slot_addr(ks), 16, L::SBO);
     const uint32_t d_t = tmem + L::s_col(q, b);
 #pragma unroll
     for (int k = 0; k < L::KSTEPS_QK; ++k) {
-      const uint32_t ao = ((k / 4) * L::Q_PANEL + (k % 4) * 32) >> 4;
-      const uint32_t bo = ((k / 4) * L::KV_PANEL + (k % 4) * 32) >> 4;
+      const uint32_t ao = ((k / L::KPP) * L::Q_PANEL + (k % L::KPP) * 32) >> 4;
+      const uint32_t bo = ((k / L::KPP) * L::KV_PANEL + (k % L::KPP) * 32) >> 4;
       mma_s(d_t, a0 + ao, b0 + bo, k > 0 ? 1u : 0u, leader);
     }
     mma_commit(bar(L::B_SFULL + q * NSB + b), leader);
@@ -396,11 +424,12 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
   // O_q (+)= P(q, b) V with V in ring slot `vs`; waits for each half of P
   // (keys [0, BN/2) then [BN/2, BN)) before issuing its K-steps.
   auto issue_pv = [&](int q, int b, int vs, bool accumulate, uint32_t pph) {
-    // bf16 V: MN-major, a 16-key K-step spans 16 rows of 128 bytes; e4m3 V^T:
-    // K-major, a 32-key K-step is 32 bytes along each 128-byte row.  Either
-    // way a K-step of P is 8 tensor-memory columns (2 bf16 or 4 e4m3 each).
-    const uint64_t b0 = F8 ? sdesc_sw128(slot_addr(vs), 16, 1024)
-                           : sdesc_sw128(slot_addr(vs), L::KV_PANEL, 1024);
+    // V as stored: MN-major, a K-step spans 16 (bf16) or 32 (e4m3) rows of
+    // SWZ bytes per column panel; e4m3 V^T: K-major, a 32-key K-step is 32
+    // bytes along each 128-byte row.  Either way a K-step of P is 8
+    // tensor-memory columns (2 bf16 or 4 e4m3 each).
+    const uint64_t b0 = L::VT ? sdesc_sw128(slot_addr(vs), 16, 1024)
+                              : sdesc_swz<L::SWZ>(slot_addr(vs), L::KV_PANEL, L::SBO);
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
 #pragma unroll
@@ -412,7 +441,7 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
       tc_fence_after_sync();
 #pragma unroll
       for (int k = h * (L::KSTEPS_PV / NH); k < (h + 1) * (L::KSTEPS_PV / NH); ++k) {
-        const uint32_t bo = F8 ? (k * 32) >> 4 : (k * 16 * 128) >> 4;
+        const uint32_t bo = L::VT ? (k * 32) >> 4 : (k * L::KEYS_PER_KSTEP * L::SWZ) >> 4;
         mma_pv(d_t, a_t + k * 8, b0 + bo, (accumulate || k > 0) ? 1u : 0u, leader);
       }
     }
@@ -595,10 +624,10 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
 __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                              const FwdParams& p, Waiter w) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, TWO>;
   constexpr int BN = L::BN, NSB = L::NSB;
   constexpr int NCH = BN / 32;  // 32-column chunks of an S row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -772,17 +801,17 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   }
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8 = false>
-__global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
+__global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO>::MIN_BLOCKS)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = Layout<D, F8>;
+  using L = Layout<D, F8, TWO>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8>(p);
+  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8, TWO>(p);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
   const Waiter w{abort_flag, p.status, p.wait_timeout_ns ? p.wait_timeout_ns : kWaitTimeoutNs};
@@ -815,18 +844,18 @@ __global__ void __launch_bounds__(Layout<D, F8>::THREADS, 1)
   // split differs per path), then meets the others at the teardown barrier.
   if (warp < 4 * L::NQ) {
     if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
-    softmax_role<D, CAUSAL, SPLIT, F8>(warp >> 2, tmem, sbase, t, p, w);
+    softmax_role<D, CAUSAL, SPLIT, F8, TWO>(warp >> 2, tmem, sbase, t, p, w);
     tc_fence_before_sync();
     __syncthreads();
   } else {
     if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
     if (warp == L::TMA_WARP || (L::SPLIT_LOAD && warp == L::V_WARP)) {
       if (lane == 0)
-        producer_role<D, CAUSAL, SPLIT, F8>(&tm_q, &tm_k, &tm_v, sbase, t, w,
+        producer_role<D, CAUSAL, SPLIT, F8, TWO>(&tm_q, &tm_k, &tm_v, sbase, t, w,
                                             warp == L::TMA_WARP ? 0 : 1, p.drop_load);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
-      mma_role<D, CAUSAL, SPLIT, F8>(tmem, sbase, t, w);
+      mma_role<D, CAUSAL, SPLIT, F8, TWO>(tmem, sbase, t, w);
       __syncwarp();
     }
     tc_fence_before_sync();

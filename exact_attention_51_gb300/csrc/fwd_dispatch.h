@@ -46,6 +46,11 @@ cudaError_t launch_combine(int d, const float* o_part, const float* lse_part, vo
 // the C ABI's per-device initialisation; nullptr if that failed).
 unsigned int* status_word();
 
+// e4m3 forward: the P.V MMA reads V as stored ([keys, d], an MN-major B
+// operand); false reads a transposed copy [d, keys] (K-major) made by a
+// separate kernel into the caller's workspace.
+constexpr bool kF8VMnMajor = true;
+
 // Largest key-split count of the split-KV entry points.
 constexpr int kMaxKvSplits = 64;
 
@@ -70,7 +75,11 @@ cudaError_t launch_transpose_v8(const void* v, void* vt, long long BH, int N, in
 
 FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();
+// two CTAs per SM, one 128-row query tile each (short rows)
+FwdVariant fwd_variant_d64_two();
+FwdVariant fwd_variant_d128_two();
 FwdVariant fwd_variant_d256();
+FwdVariant fwd_variant_e4m3_d64();
 FwdVariant fwd_variant_e4m3_d128();
 FwdVariant fwd_variant_e4m3_d256();
 

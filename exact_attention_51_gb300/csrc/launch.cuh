@@ -8,11 +8,11 @@
 
 namespace ea51 {
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8 = false>
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const FwdParams& p, cudaStream_t stream) {
-  using L = Layout<D, F8>;
-  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8>;
+  using L = Layout<D, F8, TWO>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8, TWO>;
   // The dynamic shared-memory opt-in is per device; remember which are done.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -22,6 +22,10 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    // all of the unified L1 / shared memory as shared memory, so that
+    // MIN_BLOCKS CTAs fit on an SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const unsigned grid = static_cast<unsigned>(p.n_qblk) * static_cast<unsigned>(p.BH) *
@@ -30,22 +34,22 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool TWO = false>
 cudaError_t launch_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                      const FwdParams& p, bool causal, cudaStream_t stream) {
   // split-KV partial outputs use their own instantiation, so the single-pass
   // kernel carries none of that epilogue
   if (p.kv_splits > 1)
-    return causal ? launch_one<D, true, true>(tq, tk, tv, p, stream)
-                  : launch_one<D, false, true>(tq, tk, tv, p, stream);
-  return causal ? launch_one<D, true, false>(tq, tk, tv, p, stream)
-                : launch_one<D, false, false>(tq, tk, tv, p, stream);
+    return causal ? launch_one<D, true, true, false, TWO>(tq, tk, tv, p, stream)
+                  : launch_one<D, false, true, false, TWO>(tq, tk, tv, p, stream);
+  return causal ? launch_one<D, true, false, false, TWO>(tq, tk, tv, p, stream)
+                : launch_one<D, false, false, false, TWO>(tq, tk, tv, p, stream);
 }
 
-template <int D>
+template <int D, bool TWO = false>
 FwdVariant make_variant() {
-  using L = Layout<D>;
-  return FwdVariant{L::BN, L::NQ * BM, &launch_d<D>};
+  using L = Layout<D, false, TWO>;
+  return FwdVariant{L::BN, L::NQ * BM, &launch_d<D, TWO>};
 }
 
 }  // namespace ea51

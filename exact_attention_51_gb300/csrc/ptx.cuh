@@ -207,22 +207,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 }
 
 // Instruction descriptor, kind::f8f6f4 with e4m3 A/B (format 0), fp32
-// accumulate, both operands K-major; same field positions as above.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// accumulate, A K-major, B K-major or MN-major; same field positions as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand.
+// Shared-memory matrix descriptor for an operand swizzled over SWZ = 128 or
+// 64 bytes (rows of SWZ bytes, 16-byte chunks permuted within each group of
+// eight rows, as the TMA's 128B / 64B swizzle writes them).
 //   [0,14) start >> 4, [16,30) leading byte offset >> 4, [32,46) stride byte
 //   offset >> 4, [46,48) = 1 (descriptor version), [49,52) base offset = 0
-//   (tiles start on 1024-byte boundaries), [61,64) = 2 (128B swizzle).
-// K-major: the stride offset steps over 8-row groups (1024 B); the leading
-// offset is unused.  MN-major: the leading offset steps between 64-element
-// column panels, the stride offset between 8-row groups along K.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   (tiles start on 1024-byte boundaries), [61,64) swizzle mode (2 = 128B,
+//   4 = 64B).
+// K-major: the stride offset steps over 8-row groups (8 * SWZ bytes); the
+// leading offset is unused.  MN-major: the leading offset steps between
+// SWZ-byte column panels, the stride offset between 8-row groups along K.
+template <int SWZ>
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  static_assert(SWZ == 128 || SWZ == 64, "128- or 64-byte swizzle");
+  constexpr uint64_t mode = SWZ == 128 ? 2ull : 4ull;
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (mode << 61);
+}
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return sdesc_swz<128>(saddr, lbo, sbo);
 }
 
 // Whole-warpgroup register re-allocation (all four warps must execute it).

@@ -29,7 +29,7 @@ extern "C" {
 #endif
 
 /*
- * e4m3 forward, Nq = Nk = N, d = 128 or 256.
+ * e4m3 forward, Nq = Nk = N, d = 64, 128 or 256.
  *
  *   q, k, v     e4m3 codes, one byte per element, [B,H,N,d] contiguous,
  *               16-byte aligned; read only.
@@ -39,20 +39,22 @@ extern "C" {
  *   lse         written, fp32 [B,H,N] (natural log), 4-byte aligned.
  *   scale       softmax scale (finite, >= 0), as in attn_fwd.
  *   workspace   device buffer of attn_fwd_fp8_workspace_size(B, H, N, d)
- *               bytes, 256-byte aligned: scratch for V transposed to
- *               [B*H, d, round_up(N, 16)].  o, lse and workspace must not
- *               overlap each other or q, k, v.
- * Enqueues two kernels on `stream` (the V transpose, then the fused forward)
- * and returns; status codes as in attn_fwd (d not 128 or 256, a non-positive or
- * non-finite descale, a missing or short workspace: ATTN_ERR_INVALID_ARG).
+ *               bytes, 256-byte aligned, when that size is not 0 (it is 0
+ *               in this build: the kernel reads V as stored, so NULL and 0
+ *               are accepted).  o, lse and workspace must not overlap each
+ *               other or q, k, v.
+ * Enqueues the fused forward on `stream` and returns; status codes as in
+ * attn_fwd (d not 64, 128 or 256, a non-positive or non-finite descale, a
+ * missing or short workspace: ATTN_ERR_INVALID_ARG).
  */
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q,
                           float descale_k, float descale_v, void* o, float* lse, int B, int H,
                           int N, int d, float scale, int causal, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for attn_fwd_fp8: B*H*d*round_up(N, 16), 256-byte padded
- * (0 for invalid sizes or d not 128 or 256).  Host-only. */
+/* Workspace bytes for attn_fwd_fp8: 0 when the kernel reads V as stored (this
+ * build); B*H*d*round_up(N, 16), 256-byte padded, for a build that reads a
+ * transposed copy of V; 0 for invalid sizes.  Host-only. */
 ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -67,8 +69,9 @@ ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
  *   num_splits  1..64; attn_fwd_fp8_kvcache_num_splits gives the
  *               split count the library's makespan model picks.
  *   workspace   attn_fwd_fp8_kvcache_workspace_size(B, H, Nq, Nk, d,
- *               num_splits) bytes, 256-byte aligned: V^T, then (num_splits >
- *               1) the fp32 partial O and LSE of every split.
+ *               num_splits) bytes, 256-byte aligned: (num_splits > 1) the
+ *               fp32 partial O and LSE of every split; NULL when the size is
+ *               0.
  * Other arguments, errors and asynchrony as attn_fwd_fp8; with num_splits >
  * 1 a merge kernel follows the fused kernel on `stream`.
  */

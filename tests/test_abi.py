@@ -219,32 +219,29 @@ def _fp8(lib, p, ws, ws_bytes, d=128, descales=(1.0, 1.0, 1.0), N=256):
 
 
 def test_fp8_workspace_size(lib):
-    assert ea.attn_fwd_fp8_workspace_size(1, 2, 256, 128) == 2 * 128 * 256
-    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 128) == 256 * ((128 * 32 + 255) // 256)
-    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 64) == 0
-    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 256) == 256 * ((256 * 32 + 255) // 256)
+    # the kernel reads V as stored: no workspace without split-KV
+    for d in (64, 128, 256):
+        assert ea.attn_fwd_fp8_workspace_size(1, 2, 256, d) == 0
     assert ea.attn_fwd_fp8_workspace_size(0, 1, 17, 128) == 0
+    assert ea.attn_fwd_fp8_workspace_size(1, 1, 17, 96) == 0
 
 
 def test_fp8_rejects_bad_arguments(lib):
     # every call below is invalid, so nothing is ever launched
     p = ptrs(1 << 24)
-    need = ea.attn_fwd_fp8_workspace_size(1, 2, 256, 128)
-    ws = A + (1 << 30)
-    assert _fp8(lib, p, ws, need, d=64) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, None, 0, d=96) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, None, 0, d=32) == ea.ATTN_ERR_INVALID_ARG
     for bad in [(0.0, 1.0, 1.0), (1.0, -1.0, 1.0), (1.0, 1.0, float("nan")),
                 (float("inf"), 1.0, 1.0)]:
-        assert _fp8(lib, p, ws, need, descales=bad) == ea.ATTN_ERR_INVALID_ARG
-    assert _fp8(lib, p, ws, need - 1) == ea.ATTN_ERR_INVALID_ARG
-    assert _fp8(lib, p, None, need) == ea.ATTN_ERR_INVALID_ARG
-    assert _fp8(lib, p, ws + 16, need) == ea.ATTN_ERR_MISALIGNED
-    assert _fp8(lib, p, ws, need, N=0) == ea.ATTN_ERR_INVALID_ARG
+        assert _fp8(lib, p, None, 0, descales=bad) == ea.ATTN_ERR_INVALID_ARG
+    assert _fp8(lib, p, None, 0, N=0) == ea.ATTN_ERR_INVALID_ARG
     q, k, v, o, lse = p
-    assert _fp8(lib, [q + 8, k, v, o, lse], ws, need) == ea.ATTN_ERR_MISALIGNED
+    assert _fp8(lib, [q + 8, k, v, o, lse], None, 0) == ea.ATTN_ERR_MISALIGNED
+    assert _fp8(lib, [q, k, v, o, lse + 2], None, 0, d=64) == ea.ATTN_ERR_MISALIGNED
     # o overlapping v (v spans 1*2*256*128 one-byte codes)
-    assert _fp8(lib, [q, k, v, v + 4096, lse], ws, need) == ea.ATTN_ERR_ALIAS
-    # the workspace overlapping q
-    assert _fp8(lib, p, q - (q % 256), need) == ea.ATTN_ERR_ALIAS
+    assert _fp8(lib, [q, k, v, v + 4096, lse], None, 0) == ea.ATTN_ERR_ALIAS
+    # lse overlapping o
+    assert _fp8(lib, [q, k, v, o, o + 64], None, 0) == ea.ATTN_ERR_ALIAS
 
 
 # --------------------------------------------------------------- backward
@@ -285,19 +282,25 @@ def test_fp8_kvcache_rejects_bad_arguments(lib):
                                         causal, splits, w, need if wb is None else wb, None)
 
     assert call(Nq=4097) == ea.ATTN_ERR_INVALID_ARG          # causal needs Nk >= Nq
-    assert call(d=64) == ea.ATTN_ERR_INVALID_ARG
+    assert call(d=96) == ea.ATTN_ERR_INVALID_ARG
     assert call(splits=0) == ea.ATTN_ERR_INVALID_ARG
     assert call(splits=65) == ea.ATTN_ERR_INVALID_ARG
     assert call(splits=4, wb=1024) == ea.ATTN_ERR_INVALID_ARG  # workspace too small
-    assert call(w=ws + 16) == ea.ATTN_ERR_MISALIGNED
-    assert call(w=None) == ea.ATTN_ERR_INVALID_ARG
+    assert call(splits=4, w=ws + 16) == ea.ATTN_ERR_MISALIGNED
+    assert call(splits=4, w=None) == ea.ATTN_ERR_INVALID_ARG
+    assert call(splits=4, d=64, w=None) == ea.ATTN_ERR_INVALID_ARG
+    # the split-KV workspace overlapping q
+    assert call(splits=4, w=q - (q % 256)) == ea.ATTN_ERR_ALIAS
     # o over the (longer) key tensor: keys span 1*2*4096*128 one-byte codes
     assert lib.attn_fwd_fp8_kvcache(q, k, v, 1.0, 1.0, 1.0, k + 4096, lse, 1, 2, 16, 4096, 128,
                                     0.088, 1, 1, ws, 1 << 24, None) == ea.ATTN_ERR_ALIAS
     f = ea.load_library().attn_fwd_fp8_kvcache_workspace_size
-    assert f(1, 2, 16, 4096, 128, 1) == ea.attn_fwd_fp8_workspace_size(1, 2, 4096, 128)
-    assert f(1, 2, 16, 4096, 128, 4) > f(1, 2, 16, 4096, 128, 1)
-    assert f(1, 2, 16, 4096, 64, 1) == 0
+    assert f(1, 2, 16, 4096, 128, 1) == ea.attn_fwd_fp8_workspace_size(1, 2, 4096, 128) == 0
+    # split-KV partials: splits * B*H*Nq * (d + 1) fp32, each part 256-byte padded
+    assert f(1, 2, 16, 4096, 128, 4) == (256 * ((4 * 32 * 128 * 4 + 255) // 256)
+                                         + 256 * ((4 * 32 * 4 + 255) // 256))
+    assert f(1, 2, 16, 4096, 64, 4) == ea.attn_fwd_splitkv_workspace_size(1, 2, 16, 64, 4)
+    assert f(1, 2, 16, 4096, 96, 1) == 0
     assert ea.load_library().attn_fwd_fp8_kvcache_num_splits(1, 8, 1, 32768, 128, 1, 152) >= 2
 
 

@@ -72,7 +72,7 @@ SHAPES = [(1, 2, 128), (1, 1, 1), (2, 1, 7), (1, 1, 129), (1, 2, 300), (2, 2, 25
           (1, 1, 2049)]
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("B,H,N", SHAPES, ids=[f"B{b}H{h}N{n}" for b, h, n in SHAPES])
 def test_fp8_small_shapes(B, H, N, causal, d):
@@ -85,7 +85,7 @@ def test_fp8_small_shapes(B, H, N, causal, d):
 
 
 @pytest.mark.parametrize("name,causal", [("mid", True), ("mid", False), ("long", True),
-                                         ("dsweep256", True)])
+                                         ("dsweep256", True), ("dsweep64", True)])
 def test_fp8_full_size_sampled_rows(name, causal):
     w = wl.WORKLOADS[name]
     q8, k8, v8, sc = wl.make_inputs_e4m3(w.B, w.H, w.N, w.d, w.dist, w.seed, w.k_outlier_frac)
@@ -98,7 +98,7 @@ def test_fp8_full_size_sampled_rows(name, causal):
     compare(o_s, o_ref, lse_s, lse_ref, vmax, f"{name} causal={causal} rows={len(rows)}")
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_fp8_zero_keys_exact_weights(causal, d):
     """K = 0: every visible score is 0, so every e4m3 weight is exactly 2^7
@@ -120,7 +120,7 @@ def test_fp8_zero_keys_exact_weights(causal, d):
     assert np.abs(lse - lref).max() <= 1e-3
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_fp8_single_key_returns_v(d):
     """N = 1: the one weight is exactly 2^7, so O = descale_v * V8 (exact in
     bf16: 4 significant bits times a power of two) and LSE = scale * s."""
@@ -135,7 +135,8 @@ def test_fp8_single_key_returns_v(d):
 
 
 KV_SHAPES = [(1, 2, 1, 1000, 128), (1, 2, 7, 4096, 128), (2, 1, 128, 129, 256),
-             (1, 2, 300, 300, 128), (1, 1, 513, 2000, 256), (2, 2, 16, 16384, 128)]
+             (1, 2, 300, 300, 128), (1, 1, 513, 2000, 256), (2, 2, 16, 16384, 128),
+             (1, 3, 200, 777, 64), (2, 2, 5, 3000, 64)]
 
 
 @pytest.mark.parametrize("splits", [1, None], ids=["whole", "auto-split"])
