@@ -178,17 +178,17 @@ int attn_fwd_check_args(const void* q, const void* k, const void* v, const void*
 
 namespace {
 
-// Keys per head up to which head dims 64 and 128 run the two-CTAs-per-SM
-// shape (one query tile per CTA): with few key tiles per query tile, the
-// per-CTA set-up and epilogue weigh more than sharing K/V between two query
-// tiles saves.
-constexpr int kTwoCtaMaxKeys = 2048;
+// Keys per head up to which head dim 64 runs the two-CTAs-per-SM shape (one
+// query tile per CTA): with at most 8 key tiles per query tile the per-CTA
+// set-up and epilogue weigh more than sharing K/V between two query tiles
+// saves.  Measured (GB300, both shapes on each workload): B=8 H=12 N=1024
+// causal 327 -> 354 TFLOP/s; N=8192 2-3 % slower; d = 128 10-15 % slower
+// at N = 1024..16384, so it has no two-CTA shape.
+constexpr int kTwoCtaMaxKeys = 1024;
 
 ea51::FwdVariant variant_for(int d, int Nk) {
   if (d == 64) return Nk <= kTwoCtaMaxKeys ? ea51::fwd_variant_d64_two() : ea51::fwd_variant_d64();
-  if (d == 128)
-    return Nk <= kTwoCtaMaxKeys ? ea51::fwd_variant_d128_two() : ea51::fwd_variant_d128();
-  return ea51::fwd_variant_d256();
+  return d == 128 ? ea51::fwd_variant_d128() : ea51::fwd_variant_d256();
 }
 
 // Encodes the TMA maps and launches the fused kernel; with kv_splits > 1 the
@@ -199,11 +199,12 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                unsigned long long wait_timeout_ns = 0) {
   const ea51::FwdVariant var = variant_for(d, Nk);
   const int64_t BH = static_cast<int64_t>(B) * H;
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, to;
   int rc;
   if ((rc = encode_map(&tq, q, BH, Nq, d, 128)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tk, k, BH, Nk, d, var.kv_rows)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tv, v, BH, Nk, d, var.kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&to, o, BH, Nq, d, 128)) != ATTN_OK) return rc;
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
@@ -224,7 +225,7 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   p.lse_part = lse_part;
   p.drop_load = drop_load;
   p.wait_timeout_ns = wait_timeout_ns;
-  const cudaError_t e = var.launch(&tq, &tk, &tv, p, causal != 0, stream);
+  const cudaError_t e = var.launch(&tq, &tk, &tv, &to, p, causal != 0, stream);
   if (e != cudaSuccess) return fail_cuda(e);
   return ATTN_OK;
 }
@@ -476,8 +477,9 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const ea51::FwdVariant var = fp8_variant(d);
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, to;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if ((rc = encode_map(&to, o, BH, Nq, d, 128)) != ATTN_OK) return rc;  // bf16 O (unused by e4m3 tiles)
   const int swz = d >= 128 ? 128 : d;  // one byte per element
   if ((rc = encode_tiled(&tq, q, u8, 1, BH, Nq, d, d, 128, swz)) != ATTN_OK) return rc;
   if ((rc = encode_tiled(&tk, k, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
@@ -513,7 +515,7 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
     p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off + lse_off);
   }
-  e = var.launch(&tq, &tk, &tv, p, causal != 0, st);
+  e = var.launch(&tq, &tk, &tv, &to, p, causal != 0, st);
   if (e != cudaSuccess) return fail_cuda(e);
   if (splits > 1) {
     e = ea51::launch_combine(d, p.o_part, p.lse_part, o, lse, BH * Nq, splits, st);

@@ -55,13 +55,13 @@ __global__ void __launch_bounds__(256) transpose_v8_kernel(const uint8_t* __rest
 
 template <int D>
 cudaError_t launch_e4m3(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                        const FwdParams& p, bool causal, cudaStream_t stream) {
+                        const CUtensorMap* to, const FwdParams& p, bool causal, cudaStream_t stream) {
   // split-KV partial outputs use their own instantiation, as for bf16
   if (p.kv_splits > 1)
-    return causal ? launch_one<D, true, true, true>(tq, tk, tv, p, stream)
-                  : launch_one<D, false, true, true>(tq, tk, tv, p, stream);
-  return causal ? launch_one<D, true, false, true>(tq, tk, tv, p, stream)
-                : launch_one<D, false, false, true>(tq, tk, tv, p, stream);
+    return causal ? launch_one<D, true, true, true>(tq, tk, tv, to, p, stream)
+                  : launch_one<D, false, true, true>(tq, tk, tv, to, p, stream);
+  return causal ? launch_one<D, true, false, true>(tq, tk, tv, to, p, stream)
+                : launch_one<D, false, false, true>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace

@@ -73,15 +73,16 @@ struct Shape<256> {
 struct ShapeE4M3D256 {
   static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
 };
-// Two CTAs per SM (d = 64, 128): one query tile and one S buffer per CTA, so
-// the two query tiles that take turns on the tensor core come from two CTAs.
-// Each CTA fits half the SM: 128 + D <= 256 tensor-memory columns, and Q plus
-// the K/V ring within 113 KiB of shared memory.  Short rows gain: one CTA's
-// set-up, first loads and epilogue overlap the other CTA's key tiles, and a
-// launch has twice as many, lighter CTAs to balance.
+// Two CTAs per SM (d = 64, short rows): one query tile and one S buffer per
+// CTA, so the two query tiles that take turns on the tensor core come from
+// two CTAs.  Each CTA fits half the SM: 128 + 64 <= 256 tensor-memory
+// columns, Q and a four-slot K/V ring in 80 KiB of shared memory.  Short rows
+// gain a little: one CTA's set-up, first loads and epilogue overlap the other
+// CTA's key tiles, and a launch has twice as many, lighter CTAs to balance.
 template <int D>
 struct ShapeTwo {
-  static constexpr int BN = 128, NQ = 1, NSB = 1, STAGES = D == 64 ? 4 : 2;
+  static_assert(D == 64, "two CTAs per SM: head dim 64");
+  static constexpr int BN = 128, NQ = 1, NSB = 1, STAGES = 4;
 };
 template <int D, bool F8, bool TWO>
 struct ShapeOf {
@@ -119,6 +120,8 @@ struct Layout {
   static constexpr int KEYS_PER_KSTEP = 32 / EB;  // rows of V one P.V K-step reads
   static constexpr bool VT = F8 && !kF8VMnMajor;  // V tile stored transposed
   static constexpr bool SPLIT_P = BN >= 128;  // hand P to the MMA warp in two halves
+  // bf16 O leaves through TMA stores staged in the Q buffer (same size)
+  static constexpr bool TMA_EPILOGUE = !F8;
   static constexpr int Q_PANEL = BM * SWZ;
   static constexpr int Q_BYTES = BM * D * EB;
   static constexpr int KV_PANEL = BN * SWZ;
@@ -155,15 +158,16 @@ struct Layout {
   static constexpr int THREADS = (NQ + 1) * 128;
   // Register split (setmaxnreg) when the launch budget per thread is tight:
   // 384 threads launch with 168 registers each (65536 / 384, rounded down to
-  // 8).  The control warpgroup drops to 64 and the two softmax warpgroups
-  // rise to 208: 2 * 128 * (208 - 168) = 10240 <= 128 * (168 - 64) = 13312.
+  // 8).  The control warpgroup drops to 88 and the two softmax warpgroups
+  // rise to 208: 2 * 128 * (208 - 168) = 10240 <= 128 * (168 - 88) = 10240
+  // (ptxas -v: the softmax spills below 208, the MMA / TMA roles below 88).
   // Two CTAs of 256 threads per SM launch with 128 each: control 56, softmax
   // 200, 128 * (200 - 128) = 9216 <= 128 * (128 - 56) = 9216.
   static constexpr int LAUNCH_REGS = (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8 > 255
                                          ? 255
                                          : (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8;
   static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : TWO ? 200 : 0;
-  static constexpr int REG_CONTROL = NQ == 2 ? 64 : TWO ? 56 : 0;
+  static constexpr int REG_CONTROL = NQ == 2 ? 88 : TWO ? 56 : 0;
   static_assert(REG_SOFTMAX == 0 ||
                     NQ * 128 * (REG_SOFTMAX - LAUNCH_REGS) <= 128 * (LAUNCH_REGS - REG_CONTROL),
                 "register split exceeds the launch budget");
@@ -625,7 +629,9 @@ __device__ __forceinline__ float round_bf16(float x) {
 }
 
 template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
-__device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
+// Returns true when the query tile's O has been staged in shared memory for
+// the TMA store (every thread of the tile gets the same answer).
+__device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                              const FwdParams& p, Waiter w) {
   using L = Layout<D, F8, TWO>;
   constexpr int BN = L::BN, NSB = L::NSB;
@@ -651,7 +657,7 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     if (SPLIT && grow < p.Nq)
       p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + static_cast<size_t>(t.bh) * p.Nq + grow] =
           -INFINITY;
-    return;
+    return false;
   }
   bool ok = true;
   for (int j = 0; j < n && ok; ++j) {
@@ -752,59 +758,91 @@ __device__ void softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
     }
   }
 
-  if (!ok) return;
   // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2; with split-KV the
-  // normalised fp32 partial O and the partial LSE go to the workspace.
+  // normalised fp32 partial O and the partial LSE go to the workspace.  The
+  // bf16 O tile is staged in this query tile's Q buffer -- free once o_final
+  // has completed, as no later MMA reads it -- in the 128B-swizzled layout
+  // the TMA loaded Q in, and the kernel writes it out with TMA stores of
+  // whole 128-byte row segments (coalesced; rows past Nq are not written).
+  // The e4m3 Q buffer is half the size of a bf16 O tile, so e4m3 rows are
+  // stored directly.  Warps that gave up still meet the others at the
+  // staging barrier, so no warp waits there for one that left.
   constexpr bool split_mode = SPLIT;
+  constexpr bool tma_epilogue = Layout<D, F8, TWO>::TMA_EPILOGUE && !SPLIT;
+  if constexpr (!tma_epilogue) {
+    if (!ok) return false;
+  }
   const bool valid = grow < p.Nq;
-  ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
-  if (!ok) return;
-  tc_fence_after_sync();
-  // e4m3: O and l both carry the 2^kF8Shift factor; V's dequantisation
-  // scale multiplies O.
-  const float inv_l = F8 ? p.o_scale / (l + l_fix) : 1.f / (l + l_fix);
-  const size_t row = static_cast<size_t>(t.bh) * p.Nq + (valid ? grow : 0);
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
-  float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.Nq + row) * D;
+  if constexpr (tma_epilogue) {
+    if (ok) ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
+  } else {
+    ok = warp_wait_phase(bar(L::B_OFINAL + q), 0u, w, kCodeSoftFinal);
+    if (!ok) return false;
+  }
+  if (ok) {
+    tc_fence_after_sync();
+    // e4m3: O and l both carry the 2^kF8Shift factor; V's dequantisation
+    // scale multiplies O.
+    const float inv_l = F8 ? p.o_scale / (l + l_fix) : 1.f / (l + l_fix);
+    const size_t row = static_cast<size_t>(t.bh) * p.Nq + (valid ? grow : 0);
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + row * D;
+    float* prow = p.o_part + (static_cast<size_t>(t.split) * p.BH * p.Nq + row) * D;
 #pragma unroll
-  for (int ch = 0; ch < D / 32; ++ch) {
-    uint32_t ov[32];
-    tmem_ld_32x32b_x32(o_t + ch * 32, ov);
-    tmem_ld_wait(ov);
-    if constexpr (split_mode) {
-      if (valid) {
-        float4* dst = reinterpret_cast<float4*>(prow + ch * 32);
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ov[32];
+      tmem_ld_32x32b_x32(o_t + ch * 32, ov);
+      tmem_ld_wait(ov);
+      if constexpr (split_mode) {
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(prow + ch * 32);
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4)
-          dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
-                                __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
-      }
-    } else {
-      uint32_t pk[16];
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
+                                  __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
+        }
+      } else {
+        uint32_t pk[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        if constexpr (tma_epilogue) {
+          // columns [32 ch, 32 ch + 32) are 16-byte chunks 4 (ch % 2) .. +3 of
+          // row r in 64-column panel ch / 2; chunk c sits at c ^ (r % 8)
+          const uint32_t rowb = sbase + L::OFF_Q + q * L::Q_BYTES + (ch / 2) * L::Q_PANEL + r * 128;
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4)
+            st_shared_v4(rowb + ((((ch % 2) * 4 + v4) ^ (r & 7)) << 4), pk[4 * v4], pk[4 * v4 + 1],
+                         pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
       }
     }
+    if (valid) {
+      const float lse = (m_used + __log2f(l) - (F8 ? kF8Shift : 0.f)) * kLn2;
+      if constexpr (split_mode)
+        p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + row] = lse;
+      else
+        p.lse[row] = lse;
+    }
   }
-  if (valid) {
-    const float lse = (m_used + __log2f(l) - (F8 ? kF8Shift : 0.f)) * kLn2;
-    if constexpr (split_mode)
-      p.lse_part[static_cast<size_t>(t.split) * p.BH * p.Nq + row] = lse;
-    else
-      p.lse[row] = lse;
+  if constexpr (tma_epilogue) {
+    // every writer orders its shared-memory writes before the TMA's reads;
+    // the tile's 128 threads then meet and learn whether all of them staged
+    fence_proxy_async_smem();
+    return named_barrier_and(1 + q, 128, ok);
   }
+  return false;
 }
 
 template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
 __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO>::MIN_BLOCKS)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using L = Layout<D, F8, TWO>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -830,6 +868,7 @@ __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_o);
   }
   if (warp == L::MMA_WARP) {
     tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
@@ -844,7 +883,20 @@ __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO
   // split differs per path), then meets the others at the teardown barrier.
   if (warp < 4 * L::NQ) {
     if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
-    softmax_role<D, CAUSAL, SPLIT, F8, TWO>(warp >> 2, tmem, sbase, t, p, w);
+    const int q = warp >> 2;
+    const bool staged = softmax_role<D, CAUSAL, SPLIT, F8, TWO>(q, tmem, sbase, t, p, w);
+    if (staged && (warp & 3) == 0 && lane == 0) {
+      // one lane stores the staged O panels and waits until the TMA has read
+      // them out of shared memory, before the CTA can exit (the tile's
+      // coordinates are recomputed here rather than kept through the role)
+      const Tile<D, CAUSAL, SPLIT> te = make_tile<D, CAUSAL, SPLIT, F8, TWO>(p);
+#pragma unroll
+      for (int pn = 0; pn < L::PANELS; ++pn)
+        tma_store_3d(&tm_o, sbase + L::OFF_Q + q * L::Q_BYTES + pn * L::Q_PANEL,
+                     pn * L::PANEL_ELEMS, te.row0 + q * BM, te.bh);
+      tma_store_commit();
+      tma_store_wait_read();
+    }
     tc_fence_before_sync();
     __syncthreads();
   } else {

@@ -34,8 +34,10 @@ struct FwdParams {
 struct FwdVariant {
   int kv_rows;         // keys per K/V tile (TMA box rows of K and V)
   int q_rows_per_cta;  // query rows per CTA (multiple of the 128-row Q box)
+  // tq, tk, tv: Q, K, V tiles; to: the bf16 O tensor as Q's (the epilogue's
+  // TMA stores).  The grid covers kv_splits.
   cudaError_t (*launch)(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                        const FwdParams& p, bool causal, cudaStream_t stream);  // grid covers kv_splits
+                        const CUtensorMap* to, const FwdParams& p, bool causal, cudaStream_t stream);
 };
 
 // Merges kv_splits partial results per row into bf16 O and fp32 LSE.
@@ -77,7 +79,6 @@ FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();
 // two CTAs per SM, one 128-row query tile each (short rows)
 FwdVariant fwd_variant_d64_two();
-FwdVariant fwd_variant_d128_two();
 FwdVariant fwd_variant_d256();
 FwdVariant fwd_variant_e4m3_d64();
 FwdVariant fwd_variant_e4m3_d128();

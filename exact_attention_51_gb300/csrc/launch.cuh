@@ -10,7 +10,7 @@ namespace ea51 {
 
 template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                       const FwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap* to, const FwdParams& p, cudaStream_t stream) {
   using L = Layout<D, F8, TWO>;
   auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8, TWO>;
   // The dynamic shared-memory opt-in is per device; remember which are done.
@@ -30,20 +30,20 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   }
   const unsigned grid = static_cast<unsigned>(p.n_qblk) * static_cast<unsigned>(p.BH) *
                         static_cast<unsigned>(p.kv_splits);
-  kern<<<grid, L::THREADS, L::SMEM_ALLOC, stream>>>(*tq, *tk, *tv, p);
+  kern<<<grid, L::THREADS, L::SMEM_ALLOC, stream>>>(*tq, *tk, *tv, *to, p);
   return cudaGetLastError();
 }
 
 template <int D, bool TWO = false>
 cudaError_t launch_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                     const FwdParams& p, bool causal, cudaStream_t stream) {
+                     const CUtensorMap* to, const FwdParams& p, bool causal, cudaStream_t stream) {
   // split-KV partial outputs use their own instantiation, so the single-pass
   // kernel carries none of that epilogue
   if (p.kv_splits > 1)
-    return causal ? launch_one<D, true, true, false, TWO>(tq, tk, tv, p, stream)
-                  : launch_one<D, false, true, false, TWO>(tq, tk, tv, p, stream);
-  return causal ? launch_one<D, true, false, false, TWO>(tq, tk, tv, p, stream)
-                : launch_one<D, false, false, false, TWO>(tq, tk, tv, p, stream);
+    return causal ? launch_one<D, true, true, false, TWO>(tq, tk, tv, to, p, stream)
+                  : launch_one<D, false, true, false, TWO>(tq, tk, tv, to, p, stream);
+  return causal ? launch_one<D, true, false, false, TWO>(tq, tk, tv, to, p, stream)
+                : launch_one<D, false, false, false, TWO>(tq, tk, tv, to, p, stream);
 }
 
 template <int D, bool TWO = false>
