@@ -28,6 +28,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "fwd_dispatch.h"
 #include "ptx.cuh"
@@ -119,7 +120,9 @@ struct Layout {
   static constexpr int KSTEPS_PV = BN * EB / 32;  // and of O += P V
   static constexpr int KEYS_PER_KSTEP = 32 / EB;  // rows of V one P.V K-step reads
   static constexpr bool VT = F8 && !kF8VMnMajor;  // V tile stored transposed
-  static constexpr bool SPLIT_P = BN >= 128;  // hand P to the MMA warp in two halves
+  // P is handed to the MMA warp in P_PIECES parts (32-key chunks each) so
+  // that P.V starts before the whole of P is computed
+  static constexpr int P_PIECES = BN >= 128 ? 2 : 1;
   // bf16 O leaves through TMA stores staged in the Q buffer (same size) in
   // the two-CTA shape; the others store rows directly.  Measured (GB300, A/B
   // of the same build): B=8 H=12 N=1024 d=64 causal 353 -> 368 TFLOP/s with
@@ -139,8 +142,8 @@ struct Layout {
   static constexpr int B_KVFULL = B_QFULL + NQ;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // [NQ][NSB]
-  static constexpr int B_PFULL = B_SFULL + NQ * NSB;  // [NQ][NSB][2 halves of P]
-  static constexpr int B_ODONE = B_PFULL + NQ * NSB * 2;  // [NQ]
+  static constexpr int B_PFULL = B_SFULL + NQ * NSB;  // [NQ][NSB][P_PIECES]
+  static constexpr int B_ODONE = B_PFULL + NQ * NSB * P_PIECES;  // [NQ]
   static constexpr int B_OFINAL = B_ODONE + NQ;       // [NQ]
   static constexpr int B_DRAIN = B_OFINAL + NQ;
   static constexpr int NBAR = B_DRAIN + 1;
@@ -178,6 +181,7 @@ struct Layout {
 
   static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
   static_assert(!F8 || BN == 128, "e4m3 tiles: 128 keys (one 128-byte row of V^T)");
+  static_assert((BN / 32) % P_PIECES == 0 && KSTEPS_PV % P_PIECES == 0, "P parts");
   static_assert(D * EB % SWZ == 0 && (SWZ == 128 || SWZ == 64), "row panels");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448 / MIN_BLOCKS - 1024, "shared memory budget");
@@ -441,10 +445,10 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
 #pragma unroll
-    constexpr int NH = L::SPLIT_P ? 2 : 1;
+    constexpr int NH = L::P_PIECES;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
-      if (!warp_wait_phase(bar(L::B_PFULL + (q * NSB + b) * 2 + h), pph, w, kCodeMmaP))
+      if (!warp_wait_phase(bar(L::B_PFULL + (q * NSB + b) * NH + h), pph, w, kCodeMmaP))
         return false;
       tc_fence_after_sync();
 #pragma unroll
@@ -717,37 +721,34 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       }
     }
 
-    // P = exp2(s * c - m_used) as bf16, written over the first BN/2 columns of
-    // S.  With 128-key tiles it is handed to the MMA warp in two halves, so
-    // P.V starts before the second half is computed; 64-key tiles send it
-    // whole (the second barrier round trip costs more than it overlaps).
-    constexpr int H = L::SPLIT_P ? NCH / 2 : NCH;
-    if constexpr (F8) {
-      const float m_f8 = m_used - kF8Shift;
-      l += masked ? exp_store_f8<NCH, 0, H, true>(s, lim, c, m_f8, s_t)
-                  : exp_store_f8<NCH, 0, H, false>(s, lim, c, m_f8, s_t);
-    } else {
-      l += masked ? exp_store<NCH, 0, H, true>(s, lim, c, m_used, s_t)
-                  : exp_store<NCH, 0, H, false>(s, lim, c, m_used, s_t);
-    }
-    if constexpr (L::SPLIT_P) {
+    // P = exp2(s * c - m_used) as bf16 (e4m3), written over the first BN/2
+    // (BN/4) columns of S, in P_PIECES parts: after each part's stores have
+    // completed, each warp arrives on that part's barrier, and the MMA warp
+    // issues the P.V K-steps of that part.  One part for 64-key tiles (a
+    // second barrier round trip costs more than it overlaps).
+    constexpr int CPP = NCH / L::P_PIECES;  // 32-column chunks per part
+    auto hand_part = [&](auto part) {
+      constexpr int c0 = decltype(part)::value * CPP, c1 = c0 + CPP;
+      if constexpr (F8) {
+        const float m_f8 = m_used - kF8Shift;
+        l += masked ? exp_store_f8<NCH, c0, c1, true>(s, lim, c, m_f8, s_t)
+                    : exp_store_f8<NCH, c0, c1, false>(s, lim, c, m_f8, s_t);
+      } else {
+        l += masked ? exp_store<NCH, c0, c1, true>(s, lim, c, m_used, s_t)
+                    : exp_store<NCH, c0, c1, false>(s, lim, c, m_used, s_t);
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2));
-      if constexpr (F8) {
-        const float m_f8 = m_used - kF8Shift;
-        l += masked ? exp_store_f8<NCH, H, NCH, true>(s, lim, c, m_f8, s_t)
-                    : exp_store_f8<NCH, H, NCH, false>(s, lim, c, m_f8, s_t);
-      } else {
-        l += masked ? exp_store<NCH, H, NCH, true>(s, lim, c, m_used, s_t)
-                    : exp_store<NCH, H, NCH, false>(s, lim, c, m_used, s_t);
-      }
+      if (lane == 0)
+        mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * L::P_PIECES + decltype(part)::value));
+    };
+    hand_part(std::integral_constant<int, 0>{});
+    if constexpr (L::P_PIECES > 1) hand_part(std::integral_constant<int, 1>{});
+    if constexpr (L::P_PIECES > 2) {
+      hand_part(std::integral_constant<int, 2>{});
+      hand_part(std::integral_constant<int, 3>{});
     }
-    tmem_st_wait();
-    tc_fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * 2 + (L::SPLIT_P ? 1 : 0)));
 
     // l sums the fp32 weights while P.V uses them rounded.  O's normaliser
     // takes the tile's largest weight (the one whose rounding error can be
@@ -862,7 +863,7 @@ __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO
     const uint32_t bar0 = sbase + L::OFF_BAR;
     for (int i = 0; i < L::NBAR; ++i) {
       uint32_t count = 1;
-      if (i >= L::B_PFULL && i < L::B_PFULL + L::NQ * L::NSB * 2) count = 4;  // per softmax warp
+      if (i >= L::B_PFULL && i < L::B_PFULL + L::NQ * L::NSB * L::P_PIECES) count = 4;  // per softmax warp
       mbar_init(bar0 + 8u * i, count);
     }
     *abort_flag = 0u;
