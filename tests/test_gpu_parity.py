@@ -63,6 +63,19 @@ def test_small_shapes(B, H, N, d, causal):
     check_full(q, k, v, causal, label="small")
 
 
+# head dim 64 runs two CTAs per SM with one query tile each up to 1024 keys
+# and two query tiles per CTA beyond: both shapes, with ragged tails, on
+# either side of the switch
+D64_SHAPES = [(1, 2, 1023), (1, 1, 1024), (1, 2, 1025), (2, 1, 1300), (1, 1, 2049)]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N", D64_SHAPES, ids=[f"B{b}H{h}N{n}" for b, h, n in D64_SHAPES])
+def test_d64_both_shapes(B, H, N, causal):
+    q, k, v = wl.make_inputs(B, H, N, 64, "normal", seed=3 * N + (1 if causal else 0))
+    check_full(q, k, v, causal, label="d64 shape switch")
+
+
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_tiny_workload_full_tensor(causal):
     w = wl.WORKLOADS["tiny"]
