@@ -432,14 +432,10 @@ ea51::FwdVariant fp8_variant(int d) {
                  : d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
 }
 
-// e4m3 workspace: (when V is read transposed) V^T [BH, d, round_up(Nk, 16)]
-// bytes, then (split-KV) the fp32 partial O and LSE; `part_off` receives the
-// partials' offset.
-size_t fp8_ws_bytes(int64_t BH, int Nq, int Nk, int d, int splits, size_t* part_off) {
-  const size_t nk_pad = (static_cast<size_t>(Nk) + 15) / 16 * 16;
-  const size_t vt = ea51::kF8VMnMajor ? 0 : align256(static_cast<size_t>(BH) * d * nk_pad);
-  if (part_off) *part_off = vt;
-  return vt + (splits > 1 ? splitkv_bytes(BH, Nq, d, splits, nullptr) : 0);
+// e4m3 workspace: (split-KV only) the fp32 partial O and LSE; the kernel
+// reads V as stored, so nothing else is needed.
+size_t fp8_ws_bytes(int64_t BH, int Nq, int /*Nk*/, int d, int splits) {
+  return splits > 1 ? splitkv_bytes(BH, Nq, d, splits, nullptr) : 0;
 }
 
 int fp8_general(const void* q, const void* k, const void* v, float descale_q, float descale_k,
@@ -458,8 +454,7 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
       BH * ((static_cast<int64_t>(Nk) + 127) / 128) > 0x7fffffffLL || Nk > 0x7fffffff - 16)
     return ATTN_ERR_INVALID_ARG;
   const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
-  size_t part_off = 0;
-  const size_t need = fp8_ws_bytes(BH, Nq, Nk, d, splits, &part_off);
+  const size_t need = fp8_ws_bytes(BH, Nq, Nk, d, splits);
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
   if (!al(q, 16) || !al(k, 16) || !al(v, 16) || !al(o, 16) || !al(lse, 4) ||
       (need > 0 && !al(workspace, 256)))
@@ -490,16 +485,8 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
   const int swz = d >= 128 ? 128 : d;  // one byte per element
   if ((rc = encode_tiled(&tq, q, u8, 1, BH, Nq, d, d, 128, swz)) != ATTN_OK) return rc;
   if ((rc = encode_tiled(&tk, k, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
-  if (ea51::kF8VMnMajor) {
-    // V as stored, tiled like K
-    if ((rc = encode_tiled(&tv, v, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
-  } else {
-    const int nk_pad = (Nk + 15) / 16 * 16;
-    e = ea51::launch_transpose_v8(v, workspace, BH, Nk, d, nk_pad, st);
-    if (e != cudaSuccess) return fail_cuda(e);
-    // V^T [BH, d, nk_pad]: rows are the d columns of V, keys innermost
-    if ((rc = encode_tiled(&tv, workspace, u8, 1, BH, d, Nk, nk_pad, d)) != ATTN_OK) return rc;
-  }
+  // V as stored, tiled like K (the P.V MMA reads it MN-major)
+  if ((rc = encode_tiled(&tv, v, u8, 1, BH, Nk, d, d, var.kv_rows, swz)) != ATTN_OK) return rc;
   ea51::FwdParams p{};
   p.o = o;
   p.lse = lse;
@@ -519,8 +506,8 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
   size_t lse_off = 0;
   if (splits > 1) {
     splitkv_bytes(BH, Nq, d, splits, &lse_off);
-    p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + part_off + lse_off);
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
   }
   e = var.launch(&tq, &tk, &tv, &to, p, causal != 0, st);
   if (e != cudaSuccess) return fail_cuda(e);
@@ -537,7 +524,7 @@ extern "C" {
 
 size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || !fp8_head_dim(d)) return 0;
-  return fp8_ws_bytes(static_cast<int64_t>(B) * H, N, N, d, 1, nullptr);
+  return fp8_ws_bytes(static_cast<int64_t>(B) * H, N, N, d, 1);
 }
 
 int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
@@ -550,7 +537,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
 size_t attn_fwd_fp8_kvcache_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || !fp8_head_dim(d)) return 0;
   if (num_splits < 1 || num_splits > kMaxSplits) return 0;
-  return fp8_ws_bytes(static_cast<int64_t>(B) * H, Nq, Nk, d, num_splits, nullptr);
+  return fp8_ws_bytes(static_cast<int64_t>(B) * H, Nq, Nk, d, num_splits);
 }
 
 int attn_fwd_fp8_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {

@@ -68,9 +68,9 @@ struct Shape<256> {
   static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
 };
 
-// e4m3 at d = 256: 128-key tiles (a transposed V tile needs 128-byte rows of
-// keys), one query tile, two S buffers: 2 * 128 + 256 = 512 tensor-memory
-// columns; the 8-bit K/V tiles (32 KiB) fit a four-slot ring.
+// e4m3 at d = 256: 128-key tiles, one query tile, two S buffers: 2 * 128 +
+// 256 = 512 tensor-memory columns; the 8-bit K/V tiles (32 KiB) fit a
+// four-slot ring.
 struct ShapeE4M3D256 {
   static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 2;
 };
@@ -98,9 +98,8 @@ struct ShapeOf<D, false, true> {
   using T = ShapeTwo<D>;
 };
 
-// F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots).
-// The V tile is read MN-major as stored, or (kF8VMnMajor false) from a
-// transposed copy, D rows of BN keys, as a K-major operand.
+// F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots);
+// the V tile is read MN-major as stored, as in bf16.
 template <int D, bool F8 = false, bool TWO = false>
 struct Layout {
   using Sh = typename ShapeOf<D, F8, TWO>::T;
@@ -119,7 +118,6 @@ struct Layout {
   static constexpr int KSTEPS_QK = D * EB / 32;   // 32-byte K-steps of S = Q K^T
   static constexpr int KSTEPS_PV = BN * EB / 32;  // and of O += P V
   static constexpr int KEYS_PER_KSTEP = 32 / EB;  // rows of V one P.V K-step reads
-  static constexpr bool VT = F8 && !kF8VMnMajor;  // V tile stored transposed
   // P is handed to the MMA warp in P_PIECES parts (32-key chunks each) so
   // that P.V starts before the whole of P is computed
   static constexpr int P_PIECES = BN >= 128 ? 2 : 1;
@@ -180,7 +178,7 @@ struct Layout {
                 "register split exceeds the launch budget");
 
   static_assert(D % 64 == 0 && BN % 32 == 0, "tile shape");
-  static_assert(!F8 || BN == 128, "e4m3 tiles: 128 keys (one 128-byte row of V^T)");
+  static_assert(!F8 || BN == 128, "e4m3 tiles: 128 keys");
   static_assert((BN / 32) % P_PIECES == 0 && KSTEPS_PV % P_PIECES == 0, "P parts");
   static_assert(D * EB % SWZ == 0 && (SWZ == 128 || SWZ == 64), "row panels");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
@@ -357,15 +355,10 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     mbar_arrive_expect_tx(fb, L::KV_BYTES);
     const CUtensorMap* map = (i & 1) ? tm_v : tm_k;
     const int key0 = (t.lo + (i >> 1)) * L::BN;
-    if (L::VT && (i & 1)) {
-      // transposed V: one box of D rows x BN keys (keys innermost)
-      tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES, map, fb, key0, 0, t.bh);
-    } else {
 #pragma unroll
-      for (int pn = 0; pn < L::PANELS; ++pn)
-        tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb,
-                    pn * L::PANEL_ELEMS, key0, t.bh);
-    }
+    for (int pn = 0; pn < L::PANELS; ++pn)
+      tma_load_3d(sbase + L::OFF_KV + st * L::KV_BYTES + pn * L::KV_PANEL, map, fb,
+                  pn * L::PANEL_ELEMS, key0, t.bh);
   }
   if (*w.abort_flag) {
     // Let every copy this thread started land before the CTA exits.
@@ -386,10 +379,9 @@ template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
 __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t, Waiter w) {
   using L = Layout<D, F8, TWO>;
   constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
-  // A=Q, B=K: both K-major.  A=P (tmem), B=V: MN-major in bf16, K-major for
-  // the transposed e4m3 V tile.
+  // A=Q, B=K: both K-major.  A=P (tmem), B=V: MN-major.
   constexpr uint32_t kIdescQK = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
-  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(BM, D, !L::VT) : idesc_bf16_f32(BM, D, true);
+  constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(BM, D, true) : idesc_bf16_f32(BM, D, true);
   auto mma_s = [](uint32_t d_t, uint64_t a, uint64_t b, uint32_t acc, uint32_t issue) {
     if constexpr (F8) mma_ss_f8(d_t, a, b, kIdescQK, acc, issue);
     else mma_ss(d_t, a, b, kIdescQK, acc, issue);
@@ -437,11 +429,9 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
   // (keys [0, BN/2) then [BN/2, BN)) before issuing its K-steps.
   auto issue_pv = [&](int q, int b, int vs, bool accumulate, uint32_t pph) {
     // V as stored: MN-major, a K-step spans 16 (bf16) or 32 (e4m3) rows of
-    // SWZ bytes per column panel; e4m3 V^T: K-major, a 32-key K-step is 32
-    // bytes along each 128-byte row.  Either way a K-step of P is 8
-    // tensor-memory columns (2 bf16 or 4 e4m3 each).
-    const uint64_t b0 = L::VT ? sdesc_sw128(slot_addr(vs), 16, 1024)
-                              : sdesc_swz<L::SWZ>(slot_addr(vs), L::KV_PANEL, L::SBO);
+    // SWZ bytes per column panel; a K-step of P is 8 tensor-memory columns
+    // (2 bf16 or 4 e4m3 each).
+    const uint64_t b0 = sdesc_swz<L::SWZ>(slot_addr(vs), L::KV_PANEL, L::SBO);
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
 #pragma unroll
@@ -453,7 +443,7 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
       tc_fence_after_sync();
 #pragma unroll
       for (int k = h * (L::KSTEPS_PV / NH); k < (h + 1) * (L::KSTEPS_PV / NH); ++k) {
-        const uint32_t bo = L::VT ? (k * 32) >> 4 : (k * L::KEYS_PER_KSTEP * L::SWZ) >> 4;
+        const uint32_t bo = (k * L::KEYS_PER_KSTEP * L::SWZ) >> 4;
         mma_pv(d_t, a_t + k * 8, b0 + bo, (accumulate || k > 0) ? 1u : 0u, leader);
       }
     }

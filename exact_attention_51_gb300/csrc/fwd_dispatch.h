@@ -48,11 +48,6 @@ cudaError_t launch_combine(int d, const float* o_part, const float* lse_part, vo
 // the C ABI's per-device initialisation; nullptr if that failed).
 unsigned int* status_word();
 
-// e4m3 forward: the P.V MMA reads V as stored ([keys, d], an MN-major B
-// operand); false reads a transposed copy [d, keys] (K-major) made by a
-// separate kernel into the caller's workspace.
-constexpr bool kF8VMnMajor = true;
-
 // Largest key-split count of the split-KV entry points.
 constexpr int kMaxKvSplits = 64;
 
@@ -69,11 +64,6 @@ int record_cuda_error(cudaError_t e);
 // with the kernel's bounded wait cut to `timeout_ns`.
 cudaError_t launch_wait_selftest(unsigned int* status, unsigned long long timeout_ns,
                                  cudaStream_t stream);
-
-// Transposes e4m3 V [BH, N, d] into [BH, d, n_pad] (keys innermost) for the
-// e4m3 kernel's K-major P.V operand; keys in [N, n_pad) are written as zeros.
-cudaError_t launch_transpose_v8(const void* v, void* vt, long long BH, int N, int d, int n_pad,
-                                cudaStream_t stream);
 
 FwdVariant fwd_variant_d64();
 FwdVariant fwd_variant_d128();

@@ -39,10 +39,11 @@ extern "C" {
  *   lse         written, fp32 [B,H,N] (natural log), 4-byte aligned.
  *   scale       softmax scale (finite, >= 0), as in attn_fwd.
  *   workspace   device buffer of attn_fwd_fp8_workspace_size(B, H, N, d)
- *               bytes, 256-byte aligned, when that size is not 0 (it is 0
- *               in this build: the kernel reads V as stored, so NULL and 0
- *               are accepted).  o, lse and workspace must not overlap each
- *               other or q, k, v.
+ *               bytes, 256-byte aligned, when that size is not 0.  It is 0
+ *               here (the kernel reads V as stored), so NULL and 0 are
+ *               accepted; the argument is kept so that callers need not
+ *               change if a later version needs scratch.  o, lse and
+ *               workspace must not overlap each other or q, k, v.
  * Enqueues the fused forward on `stream` and returns; status codes as in
  * attn_fwd (d not 64, 128 or 256, a non-positive or non-finite descale, a
  * missing or short workspace: ATTN_ERR_INVALID_ARG).
@@ -52,9 +53,8 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, float des
                           int N, int d, float scale, int causal, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for attn_fwd_fp8: 0 when the kernel reads V as stored (this
- * build); B*H*d*round_up(N, 16), 256-byte padded, for a build that reads a
- * transposed copy of V; 0 for invalid sizes.  Host-only. */
+/* Workspace bytes for attn_fwd_fp8: 0 (the kernel reads V as stored; 0 for
+ * invalid sizes as well).  Host-only. */
 ATTN_API size_t attn_fwd_fp8_workspace_size(int B, int H, int N, int d);
 
 /*
