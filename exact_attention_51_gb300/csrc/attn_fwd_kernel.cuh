@@ -166,13 +166,14 @@ struct Layout {
   // 8).  The control warpgroup drops to 88 and the two softmax warpgroups
   // rise to 208: 2 * 128 * (208 - 168) = 10240 <= 128 * (168 - 88) = 10240
   // (ptxas -v: the softmax spills below 208, the MMA / TMA roles below 88).
-  // Two CTAs of 256 threads per SM launch with 128 each: control 56, softmax
-  // 200, 128 * (200 - 128) = 9216 <= 128 * (128 - 56) = 9216.
+  // Two CTAs of 256 threads per SM launch with 128 each: control 48, softmax
+  // 208, 128 * (208 - 128) = 10240 <= 128 * (128 - 48) = 10240 (200 / 56
+  // spilled 32-44 bytes; 208 / 48 none).
   static constexpr int LAUNCH_REGS = (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8 > 255
                                          ? 255
                                          : (65536 / (THREADS * MIN_BLOCKS)) / 8 * 8;
-  static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : TWO ? 200 : 0;
-  static constexpr int REG_CONTROL = NQ == 2 ? 88 : TWO ? 56 : 0;
+  static constexpr int REG_SOFTMAX = NQ == 2 ? 208 : TWO ? 208 : 0;
+  static constexpr int REG_CONTROL = NQ == 2 ? 88 : TWO ? 48 : 0;
   static_assert(REG_SOFTMAX == 0 ||
                     NQ * 128 * (REG_SOFTMAX - LAUNCH_REGS) <= 128 * (LAUNCH_REGS - REG_CONTROL),
                 "register split exceeds the launch budget");
