@@ -1,6 +1,6 @@
 """Comparison of the CUDA path against the fp64 oracle.
 
-Tolerances (fixed by the spec parity bar, not derived here):
+Tolerances (the parity bar this path is held to, fixed up front, not derived here):
     max |O_gpu - O_ref|              <= 2e-2
     ||O_gpu - O_ref||_2 / ||O_ref||_2 <= 5e-3
     max |LSE_gpu - LSE_ref|          <= 1e-3
