@@ -47,6 +47,9 @@ constexpr float kRescaleThreshold = 8.0f;
 // numbers (see kF8Shift).
 constexpr float kRescaleThresholdF8 = 1.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
+// Unmasked key tiles after the first compute the first part of P with the
+// current exponent offset while the row maximum is taken (see softmax_role).
+constexpr bool kSpeculativeOffset = true;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Per-head-dim tiling.  BN = keys per tile, NQ = query tiles per CTA,
@@ -680,65 +683,89 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       if (CAUSAL) lim = min(lim, grow + p.causal_off - key0 + 1);
     }
 
-    // row maximum of the raw scores (scale >= 0 keeps the arg-max)
-    const float mx = masked ? row_max<NCH, true>(s, lim) : row_max<NCH, false>(s, lim);
-    const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
-
-    if (j == 0) {
-      m_used = (mx_c == -INFINITY) ? 0.f : mx_c;
-    } else {
-      const float m_new = fmaxf(m_used, mx_c);
-      const bool need = m_new > m_used + (F8 ? kRescaleThresholdF8 : kRescaleThreshold);
-      if (__any_sync(0xffffffffu, need)) {
-        // O holds PV(j-1) once o_done completes its phase j-1.
-        ok = warp_wait_phase(bar(L::B_ODONE + q), static_cast<uint32_t>(j - 1) & 1u, w,
-                             kCodeSoftO);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
-        if (need) m_used = m_new;
-        l *= alpha;
-        l_fix *= alpha;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t ov[32];
-          tmem_ld_32x32b_x32(o_t + ch * 32, ov);
-          tmem_ld_wait(ov);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st_32x32b_x32(o_t + ch * 32, ov);
-        }
-        tmem_st_wait();
-      }
-    }
-
     // P = exp2(s * c - m_used) as bf16 (e4m3), written over the first BN/2
     // (BN/4) columns of S, in P_PIECES parts: after each part's stores have
     // completed, each warp arrives on that part's barrier, and the MMA warp
     // issues the P.V K-steps of that part.  One part for 64-key tiles (a
     // second barrier round trip costs more than it overlaps).
     constexpr int CPP = NCH / L::P_PIECES;  // 32-column chunks per part
-    auto hand_part = [&](auto part) {
+    constexpr float kThreshold = F8 ? kRescaleThresholdF8 : kRescaleThreshold;
+    auto exp_part = [&](auto part) -> float {  // the part's weights; returns their sum
       constexpr int c0 = decltype(part)::value * CPP, c1 = c0 + CPP;
       if constexpr (F8) {
         const float m_f8 = m_used - kF8Shift;
-        l += masked ? exp_store_f8<NCH, c0, c1, true>(s, lim, c, m_f8, s_t)
-                    : exp_store_f8<NCH, c0, c1, false>(s, lim, c, m_f8, s_t);
+        return masked ? exp_store_f8<NCH, c0, c1, true>(s, lim, c, m_f8, s_t)
+                      : exp_store_f8<NCH, c0, c1, false>(s, lim, c, m_f8, s_t);
       } else {
-        l += masked ? exp_store<NCH, c0, c1, true>(s, lim, c, m_used, s_t)
-                    : exp_store<NCH, c0, c1, false>(s, lim, c, m_used, s_t);
+        return masked ? exp_store<NCH, c0, c1, true>(s, lim, c, m_used, s_t)
+                      : exp_store<NCH, c0, c1, false>(s, lim, c, m_used, s_t);
       }
+    };
+    auto hand_over = [&](int part) {
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0)
-        mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * L::P_PIECES + decltype(part)::value));
+      if (lane == 0) mbar_arrive(bar(L::B_PFULL + (q * NSB + b) * L::P_PIECES + part));
     };
-    hand_part(std::integral_constant<int, 0>{});
-    if constexpr (L::P_PIECES > 1) hand_part(std::integral_constant<int, 1>{});
+    // Moves the exponent offset to m_new where `need`: O (once P.V(j-1) has
+    // landed, o_done phase j-1) and l scale by 2^(m_used - m_new).
+    auto rescale = [&](float m_new, bool need) -> bool {
+      if (!warp_wait_phase(bar(L::B_ODONE + q), static_cast<uint32_t>(j - 1) & 1u, w, kCodeSoftO))
+        return false;
+      tc_fence_after_sync();
+      const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+      if (need) m_used = m_new;
+      l *= alpha;
+      l_fix *= alpha;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(o_t + ch * 32, ov);
+        tmem_ld_wait(ov);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+        tmem_st_32x32b_x32(o_t + ch * 32, ov);
+      }
+      tmem_st_wait();
+      return true;
+    };
+
+    // The first part of P.  Unmasked tiles after the first compute it with
+    // the current offset while the row maximum is taken (independent work
+    // the scheduler can interleave, so the maximum is off the path to the
+    // first hand-over); if the maximum grew past the threshold the part is
+    // computed again after the rescale (rare: a row's maximum settles within
+    // a few tiles).  Other tiles take the maximum first.
+    const bool speculate = kSpeculativeOffset && j > 0 && !masked;
+    float l0 = 0.f;
+    if (speculate) l0 = exp_part(std::integral_constant<int, 0>{});
+    // row maximum of the raw scores (scale >= 0 keeps the arg-max)
+    const float mx = masked ? row_max<NCH, true>(s, lim) : row_max<NCH, false>(s, lim);
+    const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
+    bool fresh = !speculate;  // part 0 still to compute
+    if (j == 0) {
+      m_used = (mx_c == -INFINITY) ? 0.f : mx_c;
+    } else {
+      const float m_new = fmaxf(m_used, mx_c);
+      const bool need = m_new > m_used + kThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        ok = rescale(m_new, need);
+        if (!ok) break;
+        fresh = true;
+      }
+    }
+    if (fresh) l0 = exp_part(std::integral_constant<int, 0>{});
+    l += l0;
+    hand_over(0);
+    if constexpr (L::P_PIECES > 1) {
+      l += exp_part(std::integral_constant<int, 1>{});
+      hand_over(1);
+    }
     if constexpr (L::P_PIECES > 2) {
-      hand_part(std::integral_constant<int, 2>{});
-      hand_part(std::integral_constant<int, 3>{});
+      l += exp_part(std::integral_constant<int, 2>{});
+      hand_over(2);
+      l += exp_part(std::integral_constant<int, 3>{});
+      hand_over(3);
     }
 
     // l sums the fp32 weights while P.V uses them rounded.  O's normaliser
