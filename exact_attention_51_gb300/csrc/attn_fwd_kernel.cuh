@@ -47,9 +47,6 @@ constexpr float kRescaleThreshold = 8.0f;
 // numbers (see kF8Shift).
 constexpr float kRescaleThresholdF8 = 1.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
-// Unmasked key tiles after the first compute the first part of P with the
-// current exponent offset while the row maximum is taken (see softmax_role).
-constexpr bool kSpeculativeOffset = true;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Per-head-dim tiling.  BN = keys per tile, NQ = query tiles per CTA,
@@ -730,19 +727,9 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       return true;
     };
 
-    // The first part of P.  Unmasked tiles after the first compute it with
-    // the current offset while the row maximum is taken (independent work
-    // the scheduler can interleave, so the maximum is off the path to the
-    // first hand-over); if the maximum grew past the threshold the part is
-    // computed again after the rescale (rare: a row's maximum settles within
-    // a few tiles).  Other tiles take the maximum first.
-    const bool speculate = kSpeculativeOffset && j > 0 && !masked;
-    float l0 = 0.f;
-    if (speculate) l0 = exp_part(std::integral_constant<int, 0>{});
     // row maximum of the raw scores (scale >= 0 keeps the arg-max)
     const float mx = masked ? row_max<NCH, true>(s, lim) : row_max<NCH, false>(s, lim);
     const float mx_c = (mx == -INFINITY) ? -INFINITY : mx * c;
-    bool fresh = !speculate;  // part 0 still to compute
     if (j == 0) {
       m_used = (mx_c == -INFINITY) ? 0.f : mx_c;
     } else {
@@ -751,11 +738,9 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
       if (__any_sync(0xffffffffu, need)) {
         ok = rescale(m_new, need);
         if (!ok) break;
-        fresh = true;
       }
     }
-    if (fresh) l0 = exp_part(std::integral_constant<int, 0>{});
-    l += l0;
+    l += exp_part(std::integral_constant<int, 0>{});
     hand_over(0);
     if constexpr (L::P_PIECES > 1) {
       l += exp_part(std::integral_constant<int, 1>{});
