@@ -12,7 +12,7 @@
 //                 S row from tensor memory, applies scale and mask, keeps the
 //                 running row max m and row sum l, writes P = exp2(x - m) as
 //                 bf16 back to tensor memory, and rescales its O row in
-//                 tensor memory when the max grew by more than 2^8.
+//                 tensor memory when the max grew by more than 2^32.
 //                 The epilogue divides by l and writes O (bf16) and LSE.
 //
 // The N x N score matrix only ever lives in tensor memory, one 128 x BN tile
@@ -37,12 +37,18 @@ namespace ea51 {
 
 constexpr int BM = 128;                      // query rows per tile (tcgen05 M)
 // log2 units: O and l are rescaled only when a row's max grows by more than
-// this; otherwise P keeps the old exponent offset (bf16 values up to 2^8).
-// A stale offset leaves a dominant weight at 2^x with x in (0, 8] instead of
-// exactly 1, so its rounding to bf16 (up to 2^-9 relative) would not cancel
-// against the fp32 normaliser; the softmax therefore gives O's normaliser
-// each tile's largest weight as rounded (see softmax_role).
-constexpr float kRescaleThreshold = 8.0f;
+// this; otherwise P keeps the old exponent offset (bf16 values up to 2^32).
+// The range is ample: O and l accumulate in fp32, so a row of N keys with
+// |V| <= Vmax stays below 2^32 * N * Vmax, far inside 2^128, and bf16 keeps
+// 8 significant bits at any exponent.  A stale offset leaves a dominant
+// weight at 2^x with x in (0, 32] instead of exactly 1, so its rounding to
+// bf16 (up to 2^-9 relative) would not cancel against the fp32 normaliser;
+// the softmax therefore gives O's normaliser each tile's largest weight as
+// rounded (see softmax_role).  Rescales cost a wait for the previous P.V and
+// a pass over O in tensor memory; with keys whose scores jump (a few keys
+// scaled by 8) a threshold of 8 rescaled some row of most warps on most
+// tiles.
+constexpr float kRescaleThreshold = 32.0f;
 // e4m3 P is 8 bits wide: a smaller threshold keeps small weights normal
 // numbers (see kF8Shift).
 constexpr float kRescaleThresholdF8 = 1.0f;

@@ -183,6 +183,24 @@ def test_peaked_rows_many_tiles(d, scale):
         check_full(q, k, v, causal, scale=scale, label=f"peaked scale={scale}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("step", [2.8, 4.2], ids=["no-rescale", "one-rescale"])
+def test_row_max_growing_tile_by_tile(d, step):
+    """Scores that grow by `step` (natural units) per 128-key tile along a
+    fixed direction: over 8 tiles a row's maximum rises by about 28 or 42
+    (log2 units), so the exponent offset stays stale for many tiles (P up to
+    about 2^28) or moves once past the rescale threshold.  Whole tensor
+    against the oracle, at scale 1."""
+    B, H, N = 1, 2, 1024
+    q, k, v = wl.make_inputs(B, H, N, d, "normal", seed=int(step * 10) + d)
+    q = (q.float() * 0.1).to(torch.bfloat16)
+    k = (k.float() * 0.1).to(torch.bfloat16)
+    q[..., 0] = 1.0
+    k[..., 0] = (step * (torch.arange(N) // 128).float()).to(torch.bfloat16).view(1, 1, N)
+    for causal in (False, True):
+        check_full(q, k, v, causal, scale=1.0, label=f"growing max step={step}")
+
+
 def test_outlier_keys_small():
     q, k, v = wl.make_inputs(1, 4, 1500, 128, "normal", seed=4321, k_outlier_frac=0.01)
     for causal in (False, True):
