@@ -351,4 +351,18 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float b0, float b1, float b2, fl
   return r;
 }
 
+// One fp32 value rounded to e4m3 (round to nearest even, saturating at
+// +-448) and back.
+__device__ __forceinline__ float round_e4m3(float x) {
+  float r;
+  asm("{\n\t.reg .b16 q;\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 q, %2, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, q;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(r)
+      : "f"(x), "f"(0.f));
+  return r;
+}
+
 }  // namespace ea51

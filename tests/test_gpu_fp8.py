@@ -101,7 +101,7 @@ def test_fp8_full_size_sampled_rows(name, causal):
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_fp8_zero_keys_exact_weights(causal, d):
-    """K = 0: every visible score is 0, so every e4m3 weight is exactly 2^7
+    """K = 0: every visible score is 0, so every e4m3 weight is exactly 2^4
     (no rounding): O_i = mean of the visible V rows, LSE_i = ln(#visible), to
     the bf16 bar."""
     B, H, N = 1, 2, 300
@@ -122,7 +122,7 @@ def test_fp8_zero_keys_exact_weights(causal, d):
 
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_fp8_single_key_returns_v(d):
-    """N = 1: the one weight is exactly 2^7, so O = descale_v * V8 (exact in
+    """N = 1: the one weight is exactly 2^4, so O = descale_v * V8 (exact in
     bf16: 4 significant bits times a power of two) and LSE = scale * s."""
     B, H, N = 2, 3, 1
     q8, k8, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=11)
