@@ -393,7 +393,8 @@ def make_path(args, w, causal, ea, dev):
         ea.attn_bwd(i["q"], i["k"], i["v"], i["o"], i["lse"], i["do"], causal=causal,
                     dq=o["dq"], dk=o["dk"], dv=o["dv"], workspace=scratch, stream=st)
     p = BenchPath("bwd", "attention bwd TFLOP/s (bf16; 2.5x the forward's algorithmic FLOPs) and % "
-                  "of GB300 dense BF16 peak", "bf16", 2.5 * w.flops(causal), 3,
+                  "of GB300 dense BF16 peak", "bf16", 2.5 * w.flops(causal), 4 if w.d == 256 else 3,
+                  "attn_bwd: row statistics + dV + dK + dQ kernels" if w.d == 256 else
                   "attn_bwd: row statistics + dK/dV + dQ kernels", 1.0,
                   {"q": q, "k": k, "v": v, "o": o_h, "lse": lse_h, "do": g},
                   lambda d: {n: torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=d)
@@ -675,8 +676,8 @@ def main(argv=None):
     causal = w.causal[-1] if args.causal == "default" else args.causal == "1"
     if args.path == "fp8" and w.d not in (64, 128, 256):
         ap.error("--path fp8 needs a d = 64, 128 or 256 workload")
-    if args.path == "bwd" and w.d not in (64, 128):
-        ap.error("--path bwd needs a d = 64 or 128 workload")
+    if args.path == "bwd" and w.d not in (64, 128, 256):
+        ap.error("--path bwd needs a d = 64, 128 or 256 workload")
     if args.impl == "reference":
         if args.steps is None:
             args.steps = 20

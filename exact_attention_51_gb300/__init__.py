@@ -395,7 +395,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     """Gradients of the forward pass: ``(dq, dk, dv)`` bf16 [B,H,N,d] for the
     upstream gradient ``dout`` of ``o``, given the forward's ``o`` and ``lse``
     (as returned by ``attn_fwd`` with the same ``causal`` and ``scale``).
-    Head dims 64 and 128.  The small fp32 workspace (2 * B*H*ceil128(N) floats)
+    Head dims 64, 128 and 256.  The small fp32 workspace (2 * B*H*ceil128(N) floats)
     is allocated with torch unless given."""
     import torch
     _check_qkv(q, k, v)

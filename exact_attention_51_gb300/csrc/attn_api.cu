@@ -567,7 +567,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   // here they are inputs, so only their sizes / alignment matter)
   int rc = check_general(q, k, v, o, lse, B, H, N, N, d, scale, causal);
   if (rc != ATTN_OK && rc != ATTN_ERR_ALIAS) return rc;
-  if (d != 64 && d != 128) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_INVALID_ARG;
   if (!dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
   const auto al = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; };
   if (!al(dout, 16) || !al(dq, 16) || !al(dk, 16) || !al(dv, 16) || !al(workspace, 256))
@@ -589,10 +589,12 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
   alignas(64) CUtensorMap tq, tk, tv, tdo;
-  if ((rc = encode_map(&tq, q, BH, N, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_map(&tk, k, BH, N, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_map(&tv, v, BH, N, d, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_map(&tdo, dout, BH, N, d, 128)) != ATTN_OK) return rc;
+  // 128-row boxes; 64 at d = 256, whose kernels stream 64-row tiles
+  const int box = d == 256 ? 64 : 128;
+  if ((rc = encode_map(&tq, q, BH, N, d, box)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, N, d, box)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, N, d, box)) != ATTN_OK) return rc;
+  if ((rc = encode_map(&tdo, dout, BH, N, d, box)) != ATTN_OK) return rc;
   ea51::BwdParams p{};
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);

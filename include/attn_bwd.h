@@ -34,12 +34,16 @@ extern "C" {
  *   dout        upstream gradient of o, bf16 [B,H,N,d]
  *   dq, dk, dv  written, bf16 [B,H,N,d]; must not overlap any input, each
  *               other or the workspace.  16-byte aligned.
- *   d           64 or 128 (tensor memory holds S, dP and two d-wide
- *               accumulators); other d is ATTN_ERR_INVALID_ARG.
+ *   d           64, 128 or 256; other d is ATTN_ERR_INVALID_ARG.  At 64 and
+ *               128 one kernel forms dK and dV together (tensor memory holds
+ *               S, dP and two d-wide accumulators); at 256 one d-wide
+ *               accumulator fills half of it, so dV, dK and dQ each take a
+ *               kernel of their own.
  *   workspace   device buffer of attn_bwd_workspace_size(B, H, N) bytes,
  *               256-byte aligned, scratch for the call (per-row D and
  *               LSE * log2 e).
- * Enqueues three kernels on `stream` (row statistics, dK/dV, dQ) and returns.
+ * Enqueues three kernels on `stream` (row statistics, dK/dV, dQ; four at
+ * d = 256: row statistics, dV, dK, dQ) and returns.
  */
 ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,

@@ -260,7 +260,8 @@ def test_bwd_rejects_bad_arguments(lib):
     def call(dd=d, w=ws, wb=need, grads=(dq, dk, dv), dout=g):
         return lib.attn_bwd(q, k, v, o, dout, lse, *grads, 1, 2, N, dd, 0.125, 1, w, wb, None)
 
-    assert call(dd=256) == ea.ATTN_ERR_INVALID_ARG
+    for bad_d in (32, 96, 192, 512):
+        assert call(dd=bad_d) == ea.ATTN_ERR_INVALID_ARG
     assert call(wb=need - 1) == ea.ATTN_ERR_INVALID_ARG
     assert call(w=None) == ea.ATTN_ERR_INVALID_ARG
     assert call(w=ws + 16) == ea.ATTN_ERR_MISALIGNED

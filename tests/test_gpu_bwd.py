@@ -56,7 +56,10 @@ def check(got, ref, label):
     return msgs
 
 
-SHAPES = [(1, 2, 128, 64), (2, 1, 300, 128), (1, 2, 513, 64), (1, 1, 1000, 128), (1, 1, 2, 64)]
+# d = 256 runs its own kernels (64-row streamed tiles): ragged against both
+# 64 and 128, a single tile, several 128-row blocks
+SHAPES = [(1, 2, 128, 64), (2, 1, 300, 128), (1, 2, 513, 64), (1, 1, 1000, 128), (1, 1, 2, 64),
+          (1, 2, 300, 256), (2, 1, 64, 256), (1, 1, 1000, 256), (1, 1, 3, 256)]
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
@@ -67,7 +70,7 @@ def test_backward_matches_oracle(B, H, N, d, causal):
     assert not msgs, "\n".join(msgs)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_single_key(d, causal):
     """N = 1: P = [1], so dV = dO and dQ = dK = 0 exactly (dS = 1*(dP - D)

@@ -11,7 +11,8 @@ these are the ones that would catch a single query tile written wrong.
 The e4m3 forward is checked the same way on its quantised inputs (tolerance
 derived in ``test_gpu_fp8.py``), and the backward on a whole head group of
 the mid workload (the heads one causal launch interleaves) and on the whole
-gpt2-shaped problem (tolerance in ``test_gpu_bwd.py``).
+gpt2-shaped problem and on the first heads of the d = 256 workload (tolerance
+in ``test_gpu_bwd.py``).
 """
 import numpy as np
 import pytest
@@ -98,3 +99,10 @@ def test_whole_tensor_backward_gpt2():
     """The gpt2-shaped workload (B=8 H=12 N=1024 d=64, causal), every head."""
     w = wl.WORKLOADS["gpt2"]
     _bwd_whole(w, True, slice(0, w.B * w.H))
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_whole_head_group_backward_dsweep256(causal):
+    """The d = 256 workload (B=4 H=16 N=8192): its three backward kernels in
+    one call, the first four heads (one causal head group) compared whole."""
+    _bwd_whole(wl.WORKLOADS["dsweep256"], causal, slice(0, 4))
