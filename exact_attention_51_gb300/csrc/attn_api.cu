@@ -589,8 +589,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
   alignas(64) CUtensorMap tq, tk, tv, tdo;
-  // 128-row boxes; 64 at d = 256, whose kernels stream 64-row tiles
-  const int box = d == 256 ? 64 : 128;
+  const int box = 128;  // 128-row blocks (at d = 256 loaded one 64-column panel at a time)
   if ((rc = encode_map(&tq, q, BH, N, d, box)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tk, k, BH, N, d, box)) != ATTN_OK) return rc;
   if ((rc = encode_map(&tv, v, BH, N, d, box)) != ATTN_OK) return rc;

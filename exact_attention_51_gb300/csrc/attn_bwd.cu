@@ -38,12 +38,6 @@ namespace ea51 {
 namespace {
 
 // Tiles of 128 query rows by 128 key rows throughout.
-// Packed bf16 output of column half h (64 fp32 columns at 64h -> 32 columns
-// of bf16 pairs at 64h): each 32-column chunk's 16 packed columns land on
-// columns this half has already read, never on the other half's.
-__host__ __device__ constexpr int packed_col(int h) { return 64 * h; }
-// tensor-memory column of the A operand (P^T, dS^T or dS) for K-step k
-__host__ __device__ constexpr int a_col(int k) { return k < 4 ? k * 8 : 64 + (k - 4) * 8; }
 
 template <int D>
 struct BwdLayout {

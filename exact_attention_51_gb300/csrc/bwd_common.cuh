@@ -18,6 +18,14 @@ constexpr int kComputeWarps = 8;
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr int kBwdThreads = 320;
 
+// 128-column tiles: packed bf16 output of column half h (64 fp32 columns at
+// 64h -> 32 columns of bf16 pairs at 64h): each 32-column chunk's 16 packed
+// columns land on columns this half has already read, never on the other
+// half's.  a_col: the tensor-memory column of K-step k (16 rows of the other
+// operand) of such a packed A operand (P^T, dS^T or dS).
+__host__ __device__ constexpr int packed_col(int h) { return 64 * h; }
+__host__ __device__ constexpr int a_col(int k) { return k < 4 ? k * 8 : 64 + (k - 4) * 8; }
+
 // Causal CTA order: heaviest blocks first (longest-processing-time order)
 // across a group of heads_per_group heads whose streamed operands fit in a
 // share of L2 (the host sizes the group); `heavy_rank` 0 is the heaviest

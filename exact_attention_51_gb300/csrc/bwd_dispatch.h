@@ -21,8 +21,8 @@ struct BwdParams {
   float scale_log2;      // scale * log2(e)
 };
 
-// Preprocess + dK/dV + dQ kernels on `stream` (d = 64, 128 or 256; at 256
-// the maps have 64-row boxes, 128 otherwise).
+// Preprocess + dK/dV + dQ kernels on `stream` (d = 64, 128 or 256; the maps
+// have 128-row boxes of 64 columns).
 cudaError_t launch_bwd(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const CUtensorMap* tdo, const BwdParams& p, const void* o, const void* dout,
                        const float* lse, int d, bool causal, cudaStream_t stream);
