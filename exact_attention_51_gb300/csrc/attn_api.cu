@@ -190,8 +190,60 @@ namespace {
 // at N = 1024..16384, so it has no two-CTA shape.
 constexpr int kTwoCtaMaxKeys = 1024;
 
-ea51::FwdVariant variant_for(int d, int Nk) {
-  if (d == 64) return Nk <= kTwoCtaMaxKeys ? ea51::fwd_variant_d64_two() : ea51::fwd_variant_d64();
+// One key-tile step of a CTA with two query tiles costs about this many
+// steps of a one-tile CTA (same SM, full grids: e4m3 d = 128 1546 vs 1306
+// TFLOP/s, bf16 d = 64 853 vs 665, i.e. 1.69 and 1.56).
+constexpr double kTwoTileStep = 1.6;
+
+// Modelled run time of a launch, in one-tile key steps: every CTA costs its
+// key tiles (split evenly over `splits` shares) times `step`, plus 2 for
+// set-up and epilogue; CTAs start heaviest first on the least-loaded SM;
+// a split launch pays 5 % for the merge kernel and the workspace traffic.
+double launch_makespan(int64_t BH, int Nq, int Nk, bool causal, int splits, int rows, int kv_rows,
+                       double step, int num_sms) {
+  const int64_t nq = (static_cast<int64_t>(Nq) + rows - 1) / rows;
+  std::vector<double> work;
+  work.reserve(static_cast<size_t>(nq * BH * splits));
+  for (int64_t qb = 0; qb < nq; ++qb) {
+    const int64_t last_key = std::min<int64_t>((qb + 1) * rows, Nq) - 1 + (Nk - Nq);
+    const int64_t tiles = causal ? last_key / kv_rows + 1 : (static_cast<int64_t>(Nk) + kv_rows - 1) / kv_rows;
+    const int64_t share = (tiles + splits - 1) / splits;
+    for (int i = 0; i < splits; ++i) {
+      const int64_t t = std::max<int64_t>(std::min<int64_t>(share, tiles - i * share), 0);
+      for (int64_t h = 0; h < BH; ++h) work.push_back(static_cast<double>(t) * step + 2.0);
+    }
+  }
+  std::sort(work.begin(), work.end(), std::greater<double>());
+  std::vector<double> sm(static_cast<size_t>(num_sms), 0.0);
+  std::make_heap(sm.begin(), sm.end(), std::greater<double>());
+  double makespan = 0;
+  for (const double wk : work) {
+    std::pop_heap(sm.begin(), sm.end(), std::greater<double>());
+    sm.back() += wk;
+    makespan = std::max(makespan, sm.back());
+    std::push_heap(sm.begin(), sm.end(), std::greater<double>());
+  }
+  return makespan * (splits > 1 ? 1.05 : 1.0);
+}
+
+// d = 64 and 128 run one query tile per CTA (two S buffers each) when the
+// default grid (two query tiles per CTA) would not fill every SM once and
+// the model above gives the one-tile grid the shorter run: twice the CTAs
+// on a half-empty GPU can outweigh what two query tiles per CTA hide (B=1
+// H=4 N=8192 d=128 causal 658 -> 992 TFLOP/s bf16, 743 -> 1117 e4m3; the
+// same shape non-causal, 128 equal CTAs, stays on the default shape).
+bool solo_shape(int64_t BH, int Nq, int Nk, bool causal, int splits, int num_sms) {
+  if (splits != 1 || BH * ((static_cast<int64_t>(Nq) + 255) / 256) >= num_sms) return false;
+  return launch_makespan(BH, Nq, Nk, causal, 1, 128, 128, 1.0, num_sms) <
+         launch_makespan(BH, Nq, Nk, causal, 1, 256, 128, kTwoTileStep, num_sms);
+}
+
+ea51::FwdVariant variant_for(int d, int Nq, int Nk, int64_t BH, bool causal, int splits,
+                             int num_sms) {
+  if (d == 64 && Nk <= kTwoCtaMaxKeys) return ea51::fwd_variant_d64_two();
+  if (d != 256 && solo_shape(BH, Nq, Nk, causal, splits, num_sms))
+    return d == 64 ? ea51::fwd_variant_d64_solo() : ea51::fwd_variant_d128_solo();
+  if (d == 64) return ea51::fwd_variant_d64();
   return d == 128 ? ea51::fwd_variant_d128() : ea51::fwd_variant_d256();
 }
 
@@ -201,8 +253,8 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, float scale, int causal, int kv_splits, float* o_part,
                float* lse_part, DeviceState* ds, cudaStream_t stream, int drop_load = -1,
                unsigned long long wait_timeout_ns = 0) {
-  const ea51::FwdVariant var = variant_for(d, Nk);
   const int64_t BH = static_cast<int64_t>(B) * H;
+  const ea51::FwdVariant var = variant_for(d, Nq, Nk, BH, causal != 0, kv_splits, ds->sms);
   alignas(64) CUtensorMap tq, tk, tv, to;
   int rc;
   if ((rc = encode_map(&tq, q, BH, Nq, d, 128)) != ATTN_OK) return rc;
@@ -294,54 +346,37 @@ int fwd_general(const void* q, const void* k, const void* v, void* o, float* lse
 }
 
 // Split count with the smallest modelled makespan (see include/attn_fwd.h).
-int split_model_for(const ea51::FwdVariant& var, int B, int H, int Nq, int Nk, int causal,
-                    int num_sms);
+int split_model_for(bool fp8, int d, int B, int H, int Nq, int Nk, int causal, int num_sms);
 
 int split_model(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128 && d != 256) || num_sms < 1)
     return 1;
   if (causal && Nk < Nq) return 1;
-  return split_model_for(variant_for(d, Nk), B, H, Nq, Nk, causal, num_sms);
+  return split_model_for(false, d, B, H, Nq, Nk, causal, num_sms);
 }
 
-// The model for the tile shape of `var` (query rows per CTA, keys per tile).
-int split_model_for(const ea51::FwdVariant& var, int B, int H, int Nq, int Nk, int causal,
-                    int num_sms) {
+ea51::FwdVariant fp8_variant(int d, int Nq, int Nk, int64_t BH, bool causal, int splits,
+                             int num_sms);
+
+// The model for the tile shape each split count launches with.
+int split_model_for(bool fp8, int d, int B, int H, int Nq, int Nk, int causal, int num_sms) {
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t nq = (static_cast<int64_t>(Nq) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
-  const int64_t ctas = BH * nq;
-  if (ctas >= num_sms) return 1;  // a full wave already: splitting only adds the merge
-  // Model: a CTA costs (key tiles it visits + 2) time units, CTAs start in
-  // launch order (heaviest first) on the least-loaded multiprocessor, and a
-  // split launch pays 5 % for the merge kernel and the workspace traffic.
-  std::vector<int64_t> work;
-  std::vector<int64_t> sm;
+  auto shape = [&](int s) {
+    return fp8 ? fp8_variant(d, Nq, Nk, BH, causal != 0, s, num_sms)
+               : variant_for(d, Nq, Nk, BH, causal != 0, s, num_sms);
+  };
+  {
+    const ea51::FwdVariant var = shape(1);
+    const int64_t nq = (static_cast<int64_t>(Nq) + var.q_rows_per_cta - 1) / var.q_rows_per_cta;
+    if (BH * nq >= num_sms) return 1;  // a full wave already: splitting only adds the merge
+  }
   double best = 0;
   int best_s = 1;
   for (int s = 1; s <= 16 && s <= kMaxSplits; ++s) {
-    work.clear();
-    for (int64_t qb = 0; qb < nq; ++qb) {
-      const int64_t last_key =
-          std::min<int64_t>((qb + 1) * var.q_rows_per_cta, Nq) - 1 + (Nk - Nq);
-      const int64_t tiles = causal ? last_key / var.kv_rows + 1
-                                   : (static_cast<int64_t>(Nk) + var.kv_rows - 1) / var.kv_rows;
-      const int64_t share = (tiles + s - 1) / s;
-      for (int i = 0; i < s; ++i) {
-        const int64_t t = std::min<int64_t>(share, tiles - i * share);
-        for (int64_t h = 0; h < BH; ++h) work.push_back(std::max<int64_t>(t, 0) + 2);
-      }
-    }
-    std::sort(work.begin(), work.end(), std::greater<int64_t>());
-    sm.assign(static_cast<size_t>(num_sms), 0);
-    std::make_heap(sm.begin(), sm.end(), std::greater<int64_t>());
-    int64_t makespan = 0;
-    for (const int64_t wk : work) {
-      std::pop_heap(sm.begin(), sm.end(), std::greater<int64_t>());
-      sm.back() += wk;
-      makespan = std::max(makespan, sm.back());
-      std::push_heap(sm.begin(), sm.end(), std::greater<int64_t>());
-    }
-    const double cost = static_cast<double>(makespan) * (s > 1 ? 1.05 : 1.0);
+    const ea51::FwdVariant var = shape(s);
+    const double step = var.q_rows_per_cta > 128 ? kTwoTileStep : 1.0;
+    const double cost = launch_makespan(BH, Nq, Nk, causal != 0, s, var.q_rows_per_cta, var.kv_rows,
+                                        step, num_sms);
     if (s == 1 || cost < best) {
       best = cost;
       best_s = s;
@@ -427,7 +462,10 @@ namespace {
 
 bool fp8_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
-ea51::FwdVariant fp8_variant(int d) {
+ea51::FwdVariant fp8_variant(int d, int Nq, int Nk, int64_t BH, bool causal, int splits,
+                             int num_sms) {
+  if (d != 256 && solo_shape(BH, Nq, Nk, causal, splits, num_sms))
+    return d == 64 ? ea51::fwd_variant_e4m3_d64_solo() : ea51::fwd_variant_e4m3_d128_solo();
   return d == 64 ? ea51::fwd_variant_e4m3_d64()
                  : d == 128 ? ea51::fwd_variant_e4m3_d128() : ea51::fwd_variant_e4m3_d256();
 }
@@ -478,7 +516,7 @@ int fp8_general(const void* q, const void* k, const void* v, float descale_q, fl
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  const ea51::FwdVariant var = fp8_variant(d);
+  const ea51::FwdVariant var = fp8_variant(d, Nq, Nk, BH, causal != 0, splits, ds->sms);
   alignas(64) CUtensorMap tq, tk, tv, to;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if ((rc = encode_map(&to, o, BH, Nq, d, 128)) != ATTN_OK) return rc;  // bf16 O (unused by e4m3 tiles)
@@ -543,7 +581,7 @@ size_t attn_fwd_fp8_kvcache_workspace_size(int B, int H, int Nq, int Nk, int d, 
 int attn_fwd_fp8_kvcache_num_splits(int B, int H, int Nq, int Nk, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || !fp8_head_dim(d) || num_sms < 1) return 1;
   if (causal && Nk < Nq) return 1;
-  return split_model_for(fp8_variant(d), B, H, Nq, Nk, causal, num_sms);
+  return split_model_for(true, d, B, H, Nq, Nk, causal, num_sms);
 }
 
 int attn_fwd_fp8_kvcache(const void* q, const void* k, const void* v, float descale_q,

@@ -3,5 +3,5 @@
 #include "launch.cuh"
 
 namespace ea51 {
-FwdVariant fwd_variant_d64_two() { return make_variant<64, true>(); }
+FwdVariant fwd_variant_d64_two() { return make_variant<64, false, kShapeTwo>(); }
 }  // namespace ea51

@@ -91,24 +91,45 @@ struct ShapeTwo {
   static_assert(D == 64, "two CTAs per SM: head dim 64");
   static constexpr int BN = 128, NQ = 1, NSB = 1, STAGES = 4;
 };
-template <int D, bool F8, bool TWO>
+// Small grids (d = 64, 128): one query tile and two S buffers per CTA, so a
+// launch whose default grid (two query tiles per CTA) would not fill the
+// GPU once has twice as many CTAs.  Two query tiles per CTA hide more of
+// each softmax where the grid is full (the default), but on a half-empty
+// grid the idle SMs cost more: B=1 H=4 N=8192 d=128 causal e4m3 743 -> 1115
+// TFLOP/s.
+template <int D>
+struct ShapeSolo {
+  static_assert(D == 64 || D == 128, "one query tile per CTA: head dim 64 or 128");
+  static constexpr int BN = 128, NQ = 1, NSB = 2, STAGES = 4;
+};
+
+// Launch shapes: the head dim's default, two CTAs per SM (d = 64 short
+// rows), one query tile per CTA (small grids).
+enum ShapeKind : int { kShapeDefault = 0, kShapeTwo = 1, kShapeSolo = 2 };
+
+template <int D, bool F8, int SK>
 struct ShapeOf {
   using T = Shape<D>;
 };
 template <>
-struct ShapeOf<256, true, false> {
+struct ShapeOf<256, true, kShapeDefault> {
   using T = ShapeE4M3D256;
 };
 template <int D>
-struct ShapeOf<D, false, true> {
+struct ShapeOf<D, false, kShapeTwo> {
   using T = ShapeTwo<D>;
+};
+template <int D, bool F8>
+struct ShapeOf<D, F8, kShapeSolo> {
+  using T = ShapeSolo<D>;
 };
 
 // F8: Q, K, V in e4m3 (8-bit tiles, half the bytes, twice the ring slots);
 // the V tile is read MN-major as stored, as in bf16.
-template <int D, bool F8 = false, bool TWO = false>
+template <int D, bool F8 = false, int SK = kShapeDefault>
 struct Layout {
-  using Sh = typename ShapeOf<D, F8, TWO>::T;
+  using Sh = typename ShapeOf<D, F8, SK>::T;
+  static constexpr bool TWO = SK == kShapeTwo;
   static constexpr int MIN_BLOCKS = TWO ? 2 : 1;  // CTAs resident per SM
   static constexpr int EB = F8 ? 1 : 2;  // bytes per Q/K/V element
   static constexpr int BN = Sh::BN, NQ = Sh::NQ, NSB = Sh::NSB,
@@ -267,9 +288,9 @@ struct Tile {
   int nkv[Shape<D>::NQ];      // key tiles [lo, lo + nkv) visited by each query tile
 };
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, int SK>
 __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) {
-  using L = Layout<D, F8, TWO>;
+  using L = Layout<D, F8, SK>;
   static_assert(L::NQ <= Shape<D>::NQ, "tile bookkeeping sized by the bf16 shape");
   Tile<D, CAUSAL, SPLIT> t;
   const int splits = SPLIT ? p.kv_splits : 1;
@@ -328,11 +349,11 @@ __device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) 
 // even number of ring slots K and V use disjoint slots, so a K tile is never
 // queued behind a V tile whose slot P.V is still reading (with one K and one
 // V slot, the next K loads during P.V and the next V during the next S).
-template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, int SK>
 __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                               Waiter w, int par, int drop_load) {
-  using L = Layout<D, F8, TWO>;
+  using L = Layout<D, F8, SK>;
   static_assert(!L::SPLIT_LOAD || L::STAGES % 2 == 0, "K and V take alternate ring slots");
   constexpr int STEP = L::SPLIT_LOAD ? 2 : 1;
   const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -382,9 +403,9 @@ __device__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 // Runs on a whole warp with warp-uniform control flow (so the descriptors
 // stay in uniform registers); one elected lane issues every tcgen05.mma and
 // tcgen05.commit.
-template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, int SK>
 __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t, Waiter w) {
-  using L = Layout<D, F8, TWO>;
+  using L = Layout<D, F8, SK>;
   constexpr int NQ = L::NQ, NSB = L::NSB, BN = L::BN;
   // A=Q, B=K: both K-major.  A=P (tmem), B=V: MN-major.
   constexpr uint32_t kIdescQK = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false);
@@ -636,12 +657,12 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8, bool TWO>
+template <int D, bool CAUSAL, bool SPLIT, bool F8, int SK>
 // Returns true when the query tile's O has been staged in shared memory for
 // the TMA store (every thread of the tile gets the same answer).
 __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SPLIT>& t,
                              const FwdParams& p, Waiter w) {
-  using L = Layout<D, F8, TWO>;
+  using L = Layout<D, F8, SK>;
   constexpr int BN = L::BN, NSB = L::NSB;
   constexpr int NCH = BN / 32;  // 32-column chunks of an S row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -788,7 +809,7 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   // stored directly.  Warps that gave up still meet the others at the
   // staging barrier, so no warp waits there for one that left.
   constexpr bool split_mode = SPLIT;
-  constexpr bool tma_epilogue = Layout<D, F8, TWO>::TMA_EPILOGUE && !SPLIT;
+  constexpr bool tma_epilogue = Layout<D, F8, SK>::TMA_EPILOGUE && !SPLIT;
   if constexpr (!tma_epilogue) {
     if (!ok) return false;
   }
@@ -858,18 +879,18 @@ __device__ bool softmax_role(int q, uint32_t tmem, uint32_t sbase, const Tile<D,
   return false;
 }
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
-__global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO>::MIN_BLOCKS)
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, int SK = kShapeDefault>
+__global__ void __launch_bounds__(Layout<D, F8, SK>::THREADS, Layout<D, F8, SK>::MIN_BLOCKS)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const FwdParams p) {
-  using L = Layout<D, F8, TWO>;
+  using L = Layout<D, F8, SK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8, TWO>(p);
+  const Tile<D, CAUSAL, SPLIT> t = make_tile<D, CAUSAL, SPLIT, F8, SK>(p);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEMSLOT);
   const Waiter w{abort_flag, p.status, p.wait_timeout_ns ? p.wait_timeout_ns : kWaitTimeoutNs};
@@ -904,12 +925,12 @@ __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO
   if (warp < 4 * L::NQ) {
     if constexpr (L::REG_SOFTMAX > 0) setmaxnreg_inc<L::REG_SOFTMAX>();
     const int q = warp >> 2;
-    const bool staged = softmax_role<D, CAUSAL, SPLIT, F8, TWO>(q, tmem, sbase, t, p, w);
+    const bool staged = softmax_role<D, CAUSAL, SPLIT, F8, SK>(q, tmem, sbase, t, p, w);
     if (staged && (warp & 3) == 0 && lane == 0) {
       // one lane stores the staged O panels and waits until the TMA has read
       // them out of shared memory, before the CTA can exit (the tile's
       // coordinates are recomputed here rather than kept through the role)
-      const Tile<D, CAUSAL, SPLIT> te = make_tile<D, CAUSAL, SPLIT, F8, TWO>(p);
+      const Tile<D, CAUSAL, SPLIT> te = make_tile<D, CAUSAL, SPLIT, F8, SK>(p);
 #pragma unroll
       for (int pn = 0; pn < L::PANELS; ++pn)
         tma_store_3d(&tm_o, sbase + L::OFF_Q + q * L::Q_BYTES + pn * L::Q_PANEL,
@@ -923,11 +944,11 @@ __global__ void __launch_bounds__(Layout<D, F8, TWO>::THREADS, Layout<D, F8, TWO
     if constexpr (L::REG_CONTROL > 0) setmaxnreg_dec<L::REG_CONTROL>();
     if (warp == L::TMA_WARP || (L::SPLIT_LOAD && warp == L::V_WARP)) {
       if (lane == 0)
-        producer_role<D, CAUSAL, SPLIT, F8, TWO>(&tm_q, &tm_k, &tm_v, sbase, t, w,
+        producer_role<D, CAUSAL, SPLIT, F8, SK>(&tm_q, &tm_k, &tm_v, sbase, t, w,
                                             warp == L::TMA_WARP ? 0 : 1, p.drop_load);
       __syncwarp();
     } else if (warp == L::MMA_WARP) {
-      mma_role<D, CAUSAL, SPLIT, F8, TWO>(tmem, sbase, t, w);
+      mma_role<D, CAUSAL, SPLIT, F8, SK>(tmem, sbase, t, w);
       __syncwarp();
     }
     tc_fence_before_sync();

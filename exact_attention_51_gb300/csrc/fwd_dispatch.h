@@ -73,5 +73,11 @@ FwdVariant fwd_variant_d256();
 FwdVariant fwd_variant_e4m3_d64();
 FwdVariant fwd_variant_e4m3_d128();
 FwdVariant fwd_variant_e4m3_d256();
+// one 128-row query tile and two S buffers per CTA (grids that the default
+// shape would leave short of one wave)
+FwdVariant fwd_variant_d64_solo();
+FwdVariant fwd_variant_d128_solo();
+FwdVariant fwd_variant_e4m3_d64_solo();
+FwdVariant fwd_variant_e4m3_d128_solo();
 
 }  // namespace ea51

@@ -8,11 +8,11 @@
 
 namespace ea51 {
 
-template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, bool TWO = false>
+template <int D, bool CAUSAL, bool SPLIT, bool F8 = false, int SK = kShapeDefault>
 cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const CUtensorMap* to, const FwdParams& p, cudaStream_t stream) {
-  using L = Layout<D, F8, TWO>;
-  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8, TWO>;
+  using L = Layout<D, F8, SK>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPLIT, F8, SK>;
   // The dynamic shared-memory opt-in is per device; remember which are done.
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -34,22 +34,22 @@ cudaError_t launch_one(const CUtensorMap* tq, const CUtensorMap* tk, const CUten
   return cudaGetLastError();
 }
 
-template <int D, bool TWO = false>
+template <int D, bool F8, int SK>
 cudaError_t launch_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                      const CUtensorMap* to, const FwdParams& p, bool causal, cudaStream_t stream) {
   // split-KV partial outputs use their own instantiation, so the single-pass
   // kernel carries none of that epilogue
   if (p.kv_splits > 1)
-    return causal ? launch_one<D, true, true, false, TWO>(tq, tk, tv, to, p, stream)
-                  : launch_one<D, false, true, false, TWO>(tq, tk, tv, to, p, stream);
-  return causal ? launch_one<D, true, false, false, TWO>(tq, tk, tv, to, p, stream)
-                : launch_one<D, false, false, false, TWO>(tq, tk, tv, to, p, stream);
+    return causal ? launch_one<D, true, true, F8, SK>(tq, tk, tv, to, p, stream)
+                  : launch_one<D, false, true, F8, SK>(tq, tk, tv, to, p, stream);
+  return causal ? launch_one<D, true, false, F8, SK>(tq, tk, tv, to, p, stream)
+                : launch_one<D, false, false, F8, SK>(tq, tk, tv, to, p, stream);
 }
 
-template <int D, bool TWO = false>
+template <int D, bool F8 = false, int SK = kShapeDefault>
 FwdVariant make_variant() {
-  using L = Layout<D, false, TWO>;
-  return FwdVariant{L::BN, L::NQ * BM, &launch_d<D, TWO>};
+  using L = Layout<D, F8, SK>;
+  return FwdVariant{L::BN, L::NQ * BM, &launch_d<D, F8, SK>};
 }
 
 }  // namespace ea51

@@ -90,11 +90,14 @@ enum attn_status {
  *
  * One thread block owns 256 query rows of one head (128 for d = 256), so a
  * launch has B*H*ceil(N/256) blocks.  When that is below the number of
- * multiprocessors (152 on GB300) -- few heads, long rows, as in decoding or
- * B=1 H=4 N=8192 -- part of the GPU idles; attn_fwd_splitkv with the count
- * from attn_fwd_splitkv_num_splits shares each block's keys over several
- * blocks instead (measured on B=1 H=4 N=8192 d=128 causal: 627 TFLOP/s here,
- * 848 with 2 splits).  For launches of a wave or more, attn_fwd is faster.
+ * multiprocessors (152 on GB300) -- few heads, long rows -- and the model
+ * of attn_fwd_splitkv_num_splits finds it faster, d = 64 and 128 run 128
+ * query rows per block instead (twice the blocks; measured on B=1 H=4
+ * N=8192 d=128 causal: 990 TFLOP/s, against 658 with 256-row blocks and 904
+ * with attn_fwd_splitkv's 2 splits).  A launch that still leaves the GPU
+ * half idle -- one or two heads, as in decoding -- runs faster through
+ * attn_fwd_splitkv with the count from attn_fwd_splitkv_num_splits, which
+ * shares each block's keys over several blocks.
  */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, void* stream);
@@ -140,9 +143,10 @@ ATTN_API int attn_fwd_splitkv(const void* q, const void* k, const void* v, void*
 ATTN_API size_t attn_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /* A split count (1..16) for attn_fwd_splitkv on a GPU with `num_sms`
- * multiprocessors: 1 when the B*H query blocks already fill one wave;
+ * multiprocessors: 1 when attn_fwd's query blocks already fill one wave;
  * otherwise the count with the shortest modelled run time (blocks cost
- * their key tiles plus a fixed overhead and start heaviest first on the
+ * their key tiles plus a fixed overhead -- a key tile of a 256-row block
+ * 1.6 times one of a 128-row block -- and start heaviest first on the
  * least-loaded multiprocessor; a split run pays 5 % for the merge).
  * Host-only. */
 ATTN_API int attn_fwd_splitkv_num_splits(int B, int H, int N, int d, int causal, int num_sms);

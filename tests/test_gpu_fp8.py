@@ -84,6 +84,22 @@ def test_fp8_small_shapes(B, H, N, causal, d):
     compare(o, o_ref, lse, lse_ref, vmax, f"{(B, H, N, d)} causal={causal}")
 
 
+# small grids run one query tile per CTA (the shapes above); enough heads for
+# the default two-tile shape, with ragged tails
+FP8_WIDE = [(1, 160, 300, 128), (1, 80, 1100, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,d", FP8_WIDE, ids=[f"B{b}H{h}N{n}d{d}" for b, h, n, d in FP8_WIDE])
+def test_fp8_default_shape_many_heads(B, H, N, d, causal):
+    q8, k8, v8, sc = wl.make_inputs_e4m3(B, H, N, d, "normal", seed=11 * N + d + (1 if causal else 0))
+    scale = 1 / math.sqrt(d)
+    o, lse = run_fp8(q8, k8, v8, sc, causal, scale)
+    o_ref, lse_ref = orc().attn_e4m3(q8, k8, v8, *sc, causal, scale)
+    vmax = float(v8.view(torch.float8_e4m3fn).double().abs().max()) * sc[2]
+    compare(o, o_ref, lse, lse_ref, vmax, f"default shape {(B, H, N, d)} causal={causal}")
+
+
 @pytest.mark.parametrize("name,causal", [("mid", True), ("mid", False), ("long", True),
                                          ("dsweep256", True), ("dsweep64", True)])
 def test_fp8_full_size_sampled_rows(name, causal):

@@ -76,6 +76,19 @@ def test_d64_both_shapes(B, H, N, causal):
     check_full(q, k, v, causal, label="d64 shape switch")
 
 
+# d = 64 and 128 run one query tile per CTA when two per CTA would not fill
+# the GPU once (the small shapes above); with enough heads the launch takes
+# the default two-tile shape: ragged tails there too
+WIDE_SHAPES = [(1, 160, 300, 128), (2, 80, 129, 128), (1, 80, 1100, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,d", WIDE_SHAPES, ids=[f"B{b}H{h}N{n}d{d}" for b, h, n, d in WIDE_SHAPES])
+def test_default_shape_many_heads(B, H, N, d, causal):
+    q, k, v = wl.make_inputs(B, H, N, d, "normal", seed=5 * N + d + (1 if causal else 0))
+    check_full(q, k, v, causal, label="default shape")
+
+
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_tiny_workload_full_tensor(causal):
     w = wl.WORKLOADS["tiny"]
