@@ -217,8 +217,12 @@ ATTN_API const char* attn_status_string(int status);
  * hanging.  This call synchronises `stream`, reads the status word of the
  * current device, clears it and returns ATTN_OK (no timeout since the last
  * call) or ATTN_ERR_TIMEOUT.  `detail`, if not NULL, receives the raw code
- * (0 when clean).  Outputs of launches that ran while the word was set are
- * not valid.
+ * (0 when clean): 0x1xx for a wait that gave up (0x101 TMA producer, 0x11x
+ * MMA warp, 0x12x elementwise / softmax warps, 0x131 draining in-flight work,
+ * 0x1f1 attn_selftest_wait_timeout), 0x1f2 when a head-dim-256 backward
+ * kernel found its shared memory not 1024-byte aligned (it then does no
+ * work), 0x1f3 when one found its ring out of order.  Outputs of launches
+ * that ran while the word was set are not valid.  attn_bwd shares the word.
  */
 ATTN_API int attn_fwd_device_status(void* stream, unsigned int* detail);
 
