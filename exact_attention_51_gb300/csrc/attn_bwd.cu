@@ -71,34 +71,59 @@ struct BwdLayout {
 
 // ------------------------------------------------------------ preprocess
 
-__global__ void bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
-                                      const __nv_bfloat16* __restrict__ dout,
-                                      const float* __restrict__ lse, float* __restrict__ lse2,
-                                      float* __restrict__ dsum, int N, int Npad, long long BH,
-                                      int d) {
-  // one warp per padded row
+// D / 8 lanes per row, each summing the 8 products of one 16-byte load of O
+// and one of dO (then a shuffle reduction over the row's lanes); 256 / D
+// rows per warp.  Padding rows (N <= i < Npad) get 0 for both.
+template <int D>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                          const float* __restrict__ lse, float* __restrict__ lse2,
+                          float* __restrict__ dsum, int N, int Npad, long long BH) {
+  constexpr int LPR = D / 8, RPW = 32 / LPR;
   const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= BH * Npad) return;
-  const long long bh = w / Npad;
-  const int i = static_cast<int>(w - bh * Npad);
+  const long long prow = w * RPW + lane / LPR;  // padded row: bh * Npad + i
+  const int sub = lane % LPR;
+  const bool live = prow < BH * Npad;
   float acc = 0.f;
   float l2 = 0.f;
-  if (i < N) {
-    const long long row = bh * N + i;
-    for (int c = lane * 2; c < d; c += 64) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + row * d + c);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(dout + row * d + c);
-      acc += __bfloat162float(a.x) * __bfloat162float(g.x) + __bfloat162float(a.y) * __bfloat162float(g.y);
+  if (live) {
+    const long long bh = prow / Npad;
+    const int i = static_cast<int>(prow - bh * Npad);
+    if (i < N) {
+      const long long row = bh * N + i;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
+      const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + sub * 8);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 af = __bfloat1622float2(a2[e]), gf = __bfloat1622float2(g2[e]);
+        acc = fmaf(af.x, gf.x, acc);
+        acc = fmaf(af.y, gf.y, acc);
+      }
+      l2 = -lse[row] * 1.4426950408889634f;
     }
-    l2 = -lse[row] * 1.4426950408889634f;
   }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    lse2[bh * Npad + i] = l2;    // -LSE * log2(e)
-    dsum[bh * Npad + i] = -acc;  // -D
+  for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (live && sub == 0) {
+    lse2[prow] = l2;    // -LSE * log2(e)
+    dsum[prow] = -acc;  // -D
   }
+}
+
+template <int D>
+cudaError_t launch_preprocess(const void* o, const void* dout, const float* lse, const BwdParams& p,
+                              cudaStream_t stream) {
+  constexpr int RPW = 32 / (D / 8);
+  const long long rows = static_cast<long long>(p.BH) * p.Npad;
+  const long long threads = (rows + RPW - 1) / RPW * 32;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  bwd_preprocess_kernel<D><<<blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, p.lse2,
+      p.dsum, p.N, p.Npad, p.BH);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ dK / dV
@@ -631,13 +656,9 @@ cudaError_t launch_bwd_d(const CUtensorMap* tq, const CUtensorMap* tk, const CUt
 cudaError_t launch_bwd(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                        const CUtensorMap* tdo, const BwdParams& p, const void* o, const void* dout,
                        const float* lse, int d, bool causal, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.BH) * p.Npad;
-  const long long threads = rows * 32;
-  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-  bwd_preprocess_kernel<<<blocks, 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, p.lse2,
-      p.dsum, p.N, p.Npad, p.BH, d);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = d == 64    ? launch_preprocess<64>(o, dout, lse, p, stream)
+                  : d == 128 ? launch_preprocess<128>(o, dout, lse, p, stream)
+                             : launch_preprocess<256>(o, dout, lse, p, stream);
   if (e != cudaSuccess) return e;
   if (d == 64) return causal ? launch_bwd_d<64, true>(tq, tk, tv, tdo, p, stream)
                              : launch_bwd_d<64, false>(tq, tk, tv, tdo, p, stream);

@@ -462,7 +462,6 @@ __device__ void mma_role(uint32_t tmem, uint32_t sbase, const Tile<D, CAUSAL, SP
     const uint64_t b0 = sdesc_swz<L::SWZ>(slot_addr(vs), L::KV_PANEL, L::SBO);
     const uint32_t d_t = tmem + L::o_col(q);
     const uint32_t a_t = tmem + L::s_col(q, b);
-#pragma unroll
     constexpr int NH = L::P_PIECES;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
