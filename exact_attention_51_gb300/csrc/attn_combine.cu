@@ -34,17 +34,31 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float wsum = 0.f;
+  // 16-byte loads where a lane's columns allow (d >= 128), two splits in
+  // flight per iteration; the branch is uniform across the warp (one row)
+#pragma unroll 2
   for (int s = 0; s < splits; ++s) {
     const float ls = lse_part[s * rows + row];
     if (ls == -INFINITY) continue;
     const float wgt = expf(ls - m);
     wsum += wgt;
     const float* src = o_part + (s * rows + row) * D + lane * PER;
+    if constexpr (PER % 4 == 0) {
 #pragma unroll
-    for (int e = 0; e < PER; e += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(src + e);
-      acc[e] += wgt * v.x;
-      acc[e + 1] += wgt * v.y;
+      for (int e = 0; e < PER; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + e);
+        acc[e] += wgt * v.x;
+        acc[e + 1] += wgt * v.y;
+        acc[e + 2] += wgt * v.z;
+        acc[e + 3] += wgt * v.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + e);
+        acc[e] += wgt * v.x;
+        acc[e + 1] += wgt * v.y;
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
