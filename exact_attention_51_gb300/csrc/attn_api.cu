@@ -283,6 +283,7 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   p.o_part = o_part;
   p.lse_part = lse_part;
   p.drop_load = drop_load;
+  p.num_sms = ds->sms;
   p.wait_timeout_ns = wait_timeout_ns;
   const cudaError_t e = var.launch(&tq, &tk, &tv, &to, p, causal != 0, stream);
   if (e != cudaSuccess) return fail_cuda(e);

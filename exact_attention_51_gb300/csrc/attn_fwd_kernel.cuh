@@ -289,13 +289,14 @@ struct Tile {
 };
 
 template <int D, bool CAUSAL, bool SPLIT, bool F8, int SK>
-__device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p) {
+__device__ __forceinline__ Tile<D, CAUSAL, SPLIT> make_tile(const FwdParams& p, int block = -1) {
   using L = Layout<D, F8, SK>;
   static_assert(L::NQ <= Shape<D>::NQ, "tile bookkeeping sized by the bf16 shape");
   Tile<D, CAUSAL, SPLIT> t;
   const int splits = SPLIT ? p.kv_splits : 1;
-  const int cta = blockIdx.x / splits;
-  t.split = blockIdx.x - cta * splits;
+  const int b = block < 0 ? static_cast<int>(blockIdx.x) : block;
+  const int cta = b / splits;
+  t.split = b - cta * splits;
   int qblk;
   if (CAUSAL) {
     // Heaviest query blocks first (longest-processing-time order) across a
@@ -909,6 +910,17 @@ __global__ void __launch_bounds__(Layout<D, F8, SK>::THREADS, Layout<D, F8, SK>:
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_o);
+    if constexpr (L::TWO && !SPLIT) {
+      // short rows: the CTA that will take this one's place in the next wave
+      // finds its Q tile in L2
+      const int next = static_cast<int>(blockIdx.x) + L::MIN_BLOCKS * p.num_sms;
+      if (p.num_sms > 0 && next < static_cast<int>(gridDim.x)) {
+        const Tile<D, CAUSAL, SPLIT> tn = make_tile<D, CAUSAL, SPLIT, F8, SK>(p, next);
+        if (tn.nkv[0] > 0)
+          for (int pn = 0; pn < L::PANELS; ++pn)
+            tma_prefetch_l2_3d(&tm_q, pn * L::PANEL_ELEMS, tn.row0, tn.bh);
+      }
+    }
   }
   if (warp == L::MMA_WARP) {
     tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);

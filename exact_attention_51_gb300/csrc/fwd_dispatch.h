@@ -29,6 +29,7 @@ struct FwdParams {
   // K/V ring position whose copy the producer leaves out in every CTA.
   int drop_load = -1;
   unsigned long long wait_timeout_ns = 0;  // limit of each bounded wait (0: about 2 s)
+  int num_sms = 0;  // multiprocessors of the device (L2 prefetch for the next wave's CTAs)
 };
 
 struct FwdVariant {
