@@ -5,8 +5,10 @@
 
 One step = one ``attn_fwd`` call over one batch of the workload (the whole
 hot path: a single fused kernel).  ``--path fp8`` times ``attn_fwd_fp8`` on
-the workload's inputs quantised to e4m3, ``--path bwd`` times ``attn_bwd``
-(the same JSON line, with their own metric names).  The default workload is the long-sequence
+the workload's inputs quantised to e4m3, ``--path bwd`` times ``attn_bwd``,
+``--path kvcache --nq Q`` times ``attn_fwd_kvcache`` with Q new queries against
+the workload's K/V as the cache (its roofline is HBM bandwidth) -- the same
+JSON line, with their own metric names.  The default workload is the long-sequence
 causal configuration the throughput target is stated on: B=1, H=32, N=16384,
 d=128, bf16, causal, Q,K,V ~ N(0,1) with 1% of the K rows scaled by 8.
 
@@ -332,6 +334,7 @@ class BenchPath:
         self.make_scratch = make_scratch    # dev -> device scratch tensor or None
         self.call = call                    # (inputs, outputs, scratch, stream) -> None
         self.out_names = out_names          # outputs copied back in the e2e loop
+        self.min_bytes = None               # HBM-bound paths: bytes read and written at least
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host_inputs.values())
@@ -342,7 +345,7 @@ def make_path(args, w, causal, ea, dev):
     scale = w.scale
     if args.path == "fwd":
         q, k, v = wl.workload_inputs(w)
-        splits = args.splits
+        splits = 1 if args.splits is None else args.splits
         if splits == 0:
             splits = ea.attn_fwd_splitkv_num_splits(
                 w.B, w.H, w.N, w.d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)
@@ -362,6 +365,36 @@ def make_path(args, w, causal, ea, dev):
                       lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
                       call, ["o", "lse"])
         p.splits = splits
+        return p
+    if args.path == "kvcache":
+        # Nq new queries against the workload's K/V as a cache of Nk = N keys
+        # (bottom-right causal), e.g. a decoding step: HBM-bound.
+        nq = args.nq
+        _, k, v = wl.workload_inputs(w)
+        q = wl.make_inputs(w.B, w.H, nq, w.d, w.dist, w.seed + 700)[0]
+        splits = 0 if args.splits is None else args.splits
+        if splits == 0:
+            splits = ea.attn_fwd_kvcache_num_splits(
+                w.B, w.H, nq, w.N, w.d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)
+        ws_bytes = ea.attn_fwd_splitkv_workspace_size(w.B, w.H, nq, w.d, splits) if splits > 1 else 0
+        # visible (query, key) pairs: query i of nq sees keys j <= i + N - nq
+        pairs = w.N * nq - (nq * (nq - 1) // 2 if causal else 0)
+
+        def call(i, o, scratch, st):
+            ea.attn_fwd_kvcache(i["q"], i["k"], i["v"], causal=causal, num_splits=splits, out=o["o"],
+                                lse=o["lse"], workspace=scratch, stream=st)
+        p = BenchPath("kvcache", f"attention fwd with a KV cache ({nq} queries against N keys) "
+                      "TFLOP/s and HBM GB/s", "bf16", 4.0 * w.B * w.H * pairs * w.d,
+                      2 if splits > 1 else 1,
+                      f"attn_fwd_kernel<{w.d},{str(causal).lower()}>" + (" + merge" if splits > 1 else ""),
+                      1.0, {"q": q, "k": k, "v": v},
+                      lambda d: {"o": torch.empty((w.B, w.H, nq, w.d), dtype=torch.bfloat16, device=d),
+                                 "lse": torch.empty((w.B, w.H, nq), dtype=torch.float32, device=d)},
+                      lambda d: torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=d),
+                      call, ["o", "lse"])
+        p.splits = splits
+        # Q, K, V read and O, LSE written once
+        p.min_bytes = w.B * w.H * (2 * nq * w.d * 2 + 2 * w.N * w.d * 2 + nq * 4)
         return p
     if args.path == "fp8":
         q8, k8, v8, sc = wl.make_inputs_e4m3(w.B, w.H, w.N, w.d, w.dist, w.seed, w.k_outlier_frac)
@@ -584,6 +617,7 @@ def run_ours(args, w, causal):
         sust_peak = peaks["bf16_tflops_sustained"] * path.peak_mult
         peak = sust_peak if sustained else burst_peak
         achieved = path.flops / (ms * 1e-3) / 1e12
+        min_bytes = path.min_bytes or (w.min_hbm_bytes() if path.name == "fwd" else None)
         traffic = load_traffic(args.workload, causal) if path.name == "fwd" else None
         q_bytes = w.B * w.H * w.N * w.d * 2
         line = {
@@ -621,11 +655,12 @@ def run_ours(args, w, causal):
                          "frac_of_sustained_peak": achieved / sust_peak,
                          "kernel": path.kernel},
             "latency_ms": percentiles(per_step),
-            "exp_bound": exp_bound(w, causal, ms, clocks, 2.0 if path.name == "bwd" else 1.0),
-            "hbm": {"min_bytes": w.min_hbm_bytes(),
-                    "achieved_gbs": w.min_hbm_bytes() / (ms * 1e-3) / 1e9,
-                    "frac": w.min_hbm_bytes() / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                    "peak_source": f"{peak_src} copy"} if path.name == "fwd" else None,
+            "exp_bound": (exp_bound(w, causal, ms, clocks, 2.0 if path.name == "bwd" else 1.0)
+                          if path.name != "kvcache" else None),
+            "hbm": {"min_bytes": min_bytes,
+                    "achieved_gbs": min_bytes / (ms * 1e-3) / 1e9,
+                    "frac": min_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "peak_source": f"{peak_src} copy"} if min_bytes else None,
             "clocks": clocks,
             "soak": {"steps": soak_steps, "seconds": t_host0 - t_soak0, "clocks": clocks_soak,
                      "what": "untimed back-to-back steps right before the timed region"},
@@ -638,6 +673,14 @@ def run_ours(args, w, causal):
         }
         if path.name == "fwd":
             line["pct_of_bf16_peak"] = line["pct_of_peak"]
+        if path.name == "kvcache":
+            # a few queries against a long cache: the bytes, not the tensor
+            # core, bound it
+            gbs = min_bytes / (ms * 1e-3) / 1e9
+            line["config"]["nq"] = args.nq
+            line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                                "peak_source": f"{peak_src} copy", "kernel": path.kernel}
         if ws == 1 and not args.no_cpu_baseline and path.name == "fwd":
             q_h, k_h, v_h = (path.host_inputs[n] for n in ("q", "k", "v"))
             tf, secs, nrows, cores = time_oracle(w, causal, q_h, k_h, v_h, args.cpu_seconds, 99)
@@ -668,12 +711,16 @@ def main(argv=None):
     ap.add_argument("--soak-seconds", type=float, default=SOAK_S,
                     help="untimed back-to-back steps right before the timed region (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=["fwd", "fp8", "bwd"], default="fwd",
+    ap.add_argument("--path", choices=["fwd", "fp8", "bwd", "kvcache"], default="fwd",
                     help="fwd: attn_fwd (bf16, the headline); fp8: attn_fwd_fp8 on the "
-                         "workload's inputs quantised to e4m3; bwd: attn_bwd")
-    ap.add_argument("--splits", type=int, default=1,
+                         "workload's inputs quantised to e4m3; bwd: attn_bwd; kvcache: "
+                         "attn_fwd_kvcache, --nq queries against the workload's K/V")
+    ap.add_argument("--nq", type=int, default=16,
+                    help="queries of the kvcache path (the workload's N is the key length)")
+    ap.add_argument("--splits", type=int, default=None,
                     help="1: attn_fwd; >1: attn_fwd_splitkv with that many key splits; "
-                         "0: attn_fwd_splitkv with its default split count")
+                         "0: the split count of the split model (default: 1 for fwd, 0 for "
+                         "kvcache)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

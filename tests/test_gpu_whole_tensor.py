@@ -106,3 +106,23 @@ def test_whole_head_group_backward_dsweep256(causal):
     """The d = 256 workload (B=4 H=16 N=8192): its three backward kernels in
     one call, the first four heads (one causal head group) compared whole."""
     _bwd_whole(wl.WORKLOADS["dsweep256"], causal, slice(0, 4))
+
+
+KV_CASES = [("long", 16), ("long", 1), ("mid", 16)]
+
+
+@pytest.mark.parametrize("name,nq", KV_CASES, ids=[f"{n}-q{q}" for n, q in KV_CASES])
+def test_whole_tensor_kvcache(name, nq):
+    """The KV-cache benchmark's shapes (nq new queries against the
+    workload's K/V as the cache, bottom-right causal, the split count
+    attn_fwd_kvcache picks): every element of O and LSE."""
+    from oracle import Oracle
+    w = wl.WORKLOADS[name]
+    _, k, v = wl.workload_inputs(w)
+    q = wl.make_inputs(w.B, w.H, nq, w.d, w.dist, w.seed + 700)[0]
+    o, lse = ea.attn_fwd_kvcache(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    _status_ok()
+    o_ref, lse_ref = Oracle().attn_bf16_qk(q, k, v, True, w.scale)
+    m = metrics(o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref)
+    record(f"whole tensor kvcache {w.describe(True)} nq={nq}", m)
+    assert within(m), f"kvcache {name} nq={nq}: {describe(m)}"
