@@ -233,6 +233,10 @@ double launch_makespan(int64_t BH, int Nq, int Nk, bool causal, int splits, int 
 // H=4 N=8192 d=128 causal 658 -> 992 TFLOP/s bf16, 743 -> 1117 e4m3; the
 // same shape non-causal, 128 equal CTAs, stays on the default shape).
 bool solo_shape(int64_t BH, int Nq, int Nk, bool causal, int splits, int num_sms) {
+  // at most one query tile (a decoding step, split-KV or not): the second
+  // tile of the default shape would have nothing to do, and two S buffers
+  // let the next tile's scores overlap this tile's softmax
+  if (Nq <= 128) return true;
   if (splits != 1 || BH * ((static_cast<int64_t>(Nq) + 255) / 256) >= num_sms) return false;
   return launch_makespan(BH, Nq, Nk, causal, 1, 128, 128, 1.0, num_sms) <
          launch_makespan(BH, Nq, Nk, causal, 1, 256, 128, kTwoTileStep, num_sms);
