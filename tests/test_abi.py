@@ -161,6 +161,25 @@ def test_splitkv_split_heuristic(lib):
         assert 1 <= f(*args, 152) <= 16
 
 
+def test_kvcache_split_heuristic(lib):
+    f = ea.attn_fwd_kvcache_num_splits
+    # a decoding step: 32 heads of one query block against 16384 cached
+    # keys leave most SMs idle, so the keys are shared out
+    assert 2 <= f(1, 32, 16, 16384, 128, True, 152) <= 16
+    assert 2 <= f(1, 32, 1, 16384, 128, True, 152) <= 16
+    # the same with enough heads to fill the GPU: no split
+    assert f(8, 32, 16, 16384, 128, True, 152) == 1
+    # the square case is the attn_fwd model
+    for args in [(1, 4, 8192, 8192, 128, True), (1, 1, 8192, 8192, 128, False)]:
+        B, H, Nq, Nk, d, c = args
+        assert f(*args, 152) == ea.attn_fwd_splitkv_num_splits(B, H, Nq, d, c, 152)
+    # causal needs Nk >= Nq; invalid shapes get 1
+    assert f(1, 1, 100, 50, 128, True, 152) == 1
+    assert f(1, 1, 16, 1024, 96, True, 152) == 1
+    # the e4m3 model runs on the same shapes
+    assert 2 <= ea.attn_fwd_fp8_kvcache_num_splits(1, 32, 16, 16384, 128, True, 152) <= 16
+
+
 def _splitkv(lib, p, splits, ws, ws_bytes, **kw):
     B, H, N, d = kw.get("B", 1), kw.get("H", 2), kw.get("N", 128), kw.get("d", 64)
     return lib.attn_fwd_splitkv(*p, B, H, N, d, 0.125, 0, splits, ws, ws_bytes, None)
