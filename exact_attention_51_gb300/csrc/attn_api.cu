@@ -186,8 +186,8 @@ namespace {
 // query tile per CTA): with at most 8 key tiles per query tile the per-CTA
 // set-up and epilogue weigh more than sharing K/V between two query tiles
 // saves.  Measured (GB300, both shapes on each workload): B=8 H=12 N=1024
-// causal 327 -> 354 TFLOP/s; N=8192 2-3 % slower; d = 128 10-15 % slower
-// at N = 1024..16384, so it has no two-CTA shape.
+// causal 327 -> 354 TFLOP/s (e4m3: 365 -> 403); N=8192 2-3 % slower; d = 128
+// 10-15 % slower at N = 1024..16384, so it has no two-CTA shape.
 constexpr int kTwoCtaMaxKeys = 1024;
 
 // One key-tile step of a CTA with two query tiles costs about this many
@@ -469,6 +469,7 @@ bool fp8_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 ea51::FwdVariant fp8_variant(int d, int Nq, int Nk, int64_t BH, bool causal, int splits,
                              int num_sms) {
+  if (d == 64 && Nk <= kTwoCtaMaxKeys) return ea51::fwd_variant_e4m3_d64_two();
   if (d != 256 && solo_shape(BH, Nq, Nk, causal, splits, num_sms))
     return d == 64 ? ea51::fwd_variant_e4m3_d64_solo() : ea51::fwd_variant_e4m3_d128_solo();
   return d == 64 ? ea51::fwd_variant_e4m3_d64()

@@ -115,8 +115,8 @@ template <>
 struct ShapeOf<256, true, kShapeDefault> {
   using T = ShapeE4M3D256;
 };
-template <int D>
-struct ShapeOf<D, false, kShapeTwo> {
+template <int D, bool F8>
+struct ShapeOf<D, F8, kShapeTwo> {
   using T = ShapeTwo<D>;
 };
 template <int D, bool F8>
@@ -211,7 +211,7 @@ struct Layout {
   static_assert(D * EB % SWZ == 0 && (SWZ == 128 || SWZ == 64), "row panels");
   static_assert(NQ * NSB * BN + NQ * D <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_ALLOC <= 232448 / MIN_BLOCKS - 1024, "shared memory budget");
-  static_assert(!TWO || (!F8 && NQ == 1 && NSB == 1), "two-CTA shape");
+  static_assert(!TWO || (NQ == 1 && NSB == 1), "two-CTA shape");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1024-byte tile alignment");
 };
 

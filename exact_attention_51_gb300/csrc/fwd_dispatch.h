@@ -74,6 +74,7 @@ FwdVariant fwd_variant_d256();
 FwdVariant fwd_variant_e4m3_d64();
 FwdVariant fwd_variant_e4m3_d128();
 FwdVariant fwd_variant_e4m3_d256();
+FwdVariant fwd_variant_e4m3_d64_two();
 // one 128-row query tile and two S buffers per CTA (grids that the default
 // shape would leave short of one wave)
 FwdVariant fwd_variant_d64_solo();
